@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step of one layer on the GB300:
+kv_append (the new token's K/V into the paged cache) + paged decode attention
+(split-KV kernel + log-sum-exp merge), on the Llama-3.1-8B-shaped workload:
+batch 32, 32 query / 8 KV heads, head_dim 128, bfloat16, every context 8192
+prefilled tokens + 1 appended (8193), 16-token blocks scattered at random in a
+shared pool.  KV read per step: 1,073,872,896 bytes (larger than the 129 MB
+L2, so no flush is needed between steps).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU float64
+oracle instead, on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
+scaling, no data-path collective); the step time is the max over ranks and
+``value`` counts the bytes of all ranks.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: KV-read GB/s (% of HBM peak), µs per layer-step"
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
+# per launch on this workload, with the hash of the kernel source it was
+# measured on; reported as null once the source has changed.
+TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": None}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="2", help="workload id (see workloads.CONFIGS)")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of untimed steps run just before the timed region "
+                         "while clocks are sampled")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, init_method="env://")
+    return dist
+
+
+def reduce_max(value, world, device):
+    """Max of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value, world, device):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for name in ("paged_decode.cu", "device_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_21_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample_case(cfg, seqs):
+    import workloads
+    spec = workloads.CONFIGS[cfg]
+    override = {"B": min(seqs, spec["B"])}
+    return workloads.make_case(cfg, device="cpu", override=override, seed=4242)
+
+
+def oracle_prepare(case):
+    import numpy as np
+    import oracle
+    from workloads import bf16_bits
+    NB, Hkv, D = case.num_blocks, case.Hkv, case.D
+    dt = np.uint16 if case.kv_dtype == 0 else np.uint8
+    kc = np.zeros((NB, Hkv, 16, D), dtype=dt)
+    vc = np.zeros_like(kc)
+    oracle.append(kc, vc, bf16_bits(case.pool_k), bf16_bits(case.pool_v),
+                  np.arange(NB * 16, dtype=np.int64), case.kv_dtype, case.k_scale, case.v_scale)
+    q64 = oracle.bf16_bits_to_f64(bf16_bits(case.q))
+    kb, vb = bf16_bits(case.k_new), bf16_bits(case.v_new)
+    return kc, vc, q64, kb, vb
+
+
+def oracle_step(case, prep):
+    """One oracle decode step on the sample: append + attention (float64)."""
+    import numpy as np
+    import oracle
+    kc, vc, q64, kb, vb = prep
+    slots = oracle.slot_mapping(case.block_tables, np.arange(case.B),
+                                case.context_lens.astype(np.int64) - 1)
+    oracle.append(kc, vc, kb, vb, slots, case.kv_dtype, case.k_scale, case.v_scale)
+    return oracle.paged_attention(q64, kc, vc, case.block_tables, case.context_lens, case.scale,
+                                  kv_dtype=case.kv_dtype, k_scale=case.k_scale,
+                                  v_scale=case.v_scale)
+
+
+def cpu_baseline(cfg, budget_s, seqs=4):
+    import oracle
+    case = oracle_sample_case(cfg, seqs)
+    prep = oracle_prepare(case)
+    oracle_step(case, prep)                       # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(case, prep)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 10000:
+            break
+    gbs = case.logical_kv_bytes() * n / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": "%d of %d sequences of this workload (%d (seq, KV head) pairs, "
+                      "%d bytes of KV per step), float64 C oracle with OpenMP, %d steps in %.1f s"
+                      % (case.B, 32 if cfg in ("2", "5a") else case.B, case.B * case.Hkv,
+                         case.logical_kv_bytes(), n, el),
+            "us_per_sample_step": el / n * 1e6}
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    import oracle
+    import workloads
+    case = oracle_sample_case(args.config, 1)
+    prep = oracle_prepare(case)
+    for _ in range(max(args.warmup, 0)):
+        oracle_step(case, prep)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(case, prep)
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    gbs = case.logical_kv_bytes() / (ms * 1e-3) / 1e9
+    spec = workloads.CONFIGS[args.config]
+    sample = ("1 of %d sequences of the workload per step (%d KV heads x %d tokens, %d bytes of "
+              "KV), float64 C oracle with OpenMP" % (spec["B"], case.Hkv,
+                                                     int(case.context_lens[0]),
+                                                     case.logical_kv_bytes()))
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args.config),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "kind": "oracle",
+                             "cores": oracle.max_threads(), "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(cfg):
+    """The workload description shared by both arms (from the recipe only)."""
+    import workloads
+    spec = workloads.CONFIGS[cfg]
+    es = 1 if spec["kv_dtype"] == workloads.FP8_E4M3 else 2
+    c = {"workload": spec["desc"], "config_id": cfg, "batch": spec["B"],
+         "q_heads": spec["Hq"], "kv_heads": spec["Hkv"], "head_dim": spec["D"],
+         "kv_dtype": "e4m3" if es == 1 else "bf16", "block_size": 16,
+         "l2": "inputs larger than L2: the KV read per step exceeds the 129 MB L2, no flush"}
+    if "N" in spec:
+        c["context_after_append"] = spec["N"] + 1
+        c["kv_bytes_per_step"] = 2 * spec["B"] * (spec["N"] + 1) * spec["Hkv"] * spec["D"] * es
+    return c
+
+
+# -------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+
+    import paged_kv_cache_21_gb300 as pk
+    import workloads
+
+    cfg = args.config
+    case = workloads.make_case(cfg, device=device)
+    B, Hq, Hkv, D = case.B, case.Hq, case.Hkv, case.D
+    NB = case.num_blocks
+    cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
+    kc = torch.empty((NB, Hkv, 16, D), dtype=cdt, device=device)
+    vc = torch.empty_like(kc)
+    pk.kv_append(case.pool_k, case.pool_v, kc, vc,
+                 torch.arange(NB * 16, dtype=torch.int64, device=device),
+                 case.k_scale, case.v_scale)
+    case.pool_k = case.pool_v = None
+    torch.cuda.synchronize()
+
+    slots_np = pk.slot_mapping(case.block_tables, case.context_lens.astype(np.int64) - 1)
+    slots = torch.from_numpy(slots_np).to(device)
+    bt = torch.from_numpy(case.block_tables).to(device)
+    cl = torch.from_numpy(case.context_lens).to(device)
+    q, k_new, v_new = case.q, case.k_new, case.v_new
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+    ws = pk.alloc_workspace(B, Hq, Hkv, D, case.kv_dtype, device=device)
+    stream = torch.cuda.current_stream(device)
+    kv_bytes = case.logical_kv_bytes()
+
+    def step(evs=None):
+        pk.kv_append(k_new, v_new, kc, vc, slots, case.k_scale, case.v_scale, stream=stream)
+        if evs is None:
+            pk.paged_decode_attention(out, q, kc, vc, bt, cl, case.scale, ws,
+                                      case.k_scale, case.v_scale, stream=stream)
+        else:
+            pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
+                                            case.k_scale, case.v_scale, stream=stream)
+
+    # warm-up (W >= 3), then a short untimed soak while the clock sampler runs
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+    # timed region: exactly K steps
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e in ev:                      # create the event handles before the timed region
+        for x in e:
+            x.record(stream)
+    t_beg = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_beg.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step(ev[i][1:])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+
+    ms_local = t_beg.elapsed_time(t_end) / K
+    append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    split_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    combine_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(K))
+    ms = reduce_max(ms_local, world, device)
+    total_bytes = reduce_sum(float(kv_bytes), world, device)
+    value = total_bytes / (ms * 1e-3) / 1e9
+    flags, detail = pk.get_device_error()
+    assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (pinned), append + attention, D2H of the output, every step
+    e2e = None
+    if not args.no_e2e:
+        h_q = q.cpu().pin_memory()
+        h_k = k_new.cpu().pin_memory()
+        h_v = v_new.cpu().pin_memory()
+        h_slots = torch.from_numpy(slots_np).pin_memory()
+        h_bt = torch.from_numpy(case.block_tables).pin_memory()
+        h_cl = torch.from_numpy(case.context_lens).pin_memory()
+        h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+        d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            d_q.copy_(h_q, non_blocking=True)
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            d_slots.copy_(h_slots, non_blocking=True)
+            d_bt.copy_(h_bt, non_blocking=True)
+            d_cl.copy_(h_cl, non_blocking=True)
+            pk.kv_append(d_k, d_v, kc, vc, d_slots, case.k_scale, case.v_scale, stream=stream)
+            pk.paged_decode_attention(out, d_q, kc, vc, d_bt, d_cl, case.scale, ws,
+                                      case.k_scale, case.v_scale, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(max(args.warmup, 3)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = reduce_max(e0.elapsed_time(e1) / K, world, device)
+        e2e = {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (split_ms * 1e-3) / 1e9
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256"] == kernel_sha() else None
+    roofline = {"bound": "hbm", "kernel": "paged_decode_split_kernel<128,bf16>",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
+                "split_us": split_ms * 1e3, "combine_us": combine_ms * 1e3,
+                "append_us": append_ms * 1e3}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "us_per_layer_step": ms * 1e3, "pct_of_hbm_peak": 100.0 * (kv_bytes / (ms * 1e-3)
+                                                                      / 1e9) / peak,
+            "pct_of_8tbs_nameplate": 100.0 * (kv_bytes / (ms * 1e-3) / 1e9) / 8000.0,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if case.kv_dtype == workloads.BF16 else "e4m3",
+            "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
+            "config": dict(workload_config(cfg),
+                           parallelism="replicas x%d" % world if world > 1 else "single GPU"),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

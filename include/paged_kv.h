@@ -1,0 +1,254 @@
+/*
+ * paged_kv.h -- C ABI of the GB300 paged KV-cache decode library (libpagedkv.so).
+ *
+ * One decode step of one layer is
+ *     kv_step (host)  ->  kv_append (GPU)  ->  paged_decode_attention (GPU)
+ * i.e. the new token's K/V is appended to the cache first and the new query
+ * then attends over the whole cache, including itself ("Transformer
+ * attention mask and KV cache inference", section "Prefill and decode
+ * phases").
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns an int status: KV_OK (0) or a negative KV_ERR_*.
+ *     Nothing throws across this boundary.
+ *   - Device buffers are plain device pointers owned by the caller; the
+ *     library never allocates, frees or retains device memory.  Host
+ *     buffers are plain host pointers, also caller-owned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  GPU entry points only enqueue work and return; a launch
+ *     failure is reported as KV_ERR_CUDA.  Faults found by the kernels'
+ *     own bounds checks (a slot or block id outside the pool, a context
+ *     longer than its block-table row) do not abort: the offending access
+ *     is skipped (or reads zeros) and a sticky device flag is set that
+ *     kv_get_device_error() returns.
+ *   - Cache layout, per layer: k_cache and v_cache are each
+ *     [num_blocks][num_kv_heads][16][head_dim] elements of kv_dtype,
+ *     row-major.  One (block, head) tile is 16*head_dim*elem_bytes
+ *     contiguous bytes.  The 16-token block is the page of "KV Cache, Flash
+ *     Attention and inference optimization", section "PagedAttention", and
+ *     the [heads, seq, head_dim] order inside it is the tensor shape of "KV
+ *     Cache" (heepie.pages.dev), section "Tensor".
+ *   - Supported shapes: head_dim 64 or 128; num_q_heads a multiple of
+ *     num_kv_heads with group size G = num_q_heads / num_kv_heads in 1..8
+ *     ("KV cache complete guide", section "(2) GQA": MHA G=1, GQA, MQA).
+ *     Query head h reads KV head h / G.
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define KV_OK 0
+#define KV_ERR_INVALID_ARG (-1)   /* bad pointer, size, shape or id */
+#define KV_ERR_OUT_OF_BLOCKS (-2) /* the block pool cannot satisfy the request */
+#define KV_ERR_UNSUPPORTED (-3)   /* valid but not implemented (head_dim, group size) */
+#define KV_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
+#define KV_ERR_NOT_FOUND (-5)     /* unknown sequence id */
+#define KV_ERR_EXISTS (-6)        /* sequence id already present */
+
+/* --------------------------------------------------------------- data types */
+#define KV_DTYPE_BF16 0     /* bfloat16 */
+#define KV_DTYPE_FP8_E4M3 1 /* OCP E4M3 ("fn"), per-tensor scale: x = code * scale */
+#define KV_DTYPE_F32 2      /* float32 (attention output only) */
+
+#define KV_BLOCK_SIZE 16
+
+/* Device error flags reported by kv_get_device_error(). */
+#define KV_DEVERR_SLOT_OUT_OF_RANGE 1     /* kv_append: slot >= num_blocks*16 */
+#define KV_DEVERR_BLOCK_OUT_OF_RANGE 2    /* a block-table entry outside [0, num_blocks) */
+#define KV_DEVERR_CONTEXT_TOO_LONG 4      /* context_lens[s] > 16*max_blocks_per_seq, or < 0 */
+#define KV_DEVERR_PIPELINE_TIMEOUT 8      /* a bulk copy never arrived (a bug, never expected) */
+
+/* ------------------------------------------------------------------ sizing */
+
+/* Bytes of K plus V for a whole model:
+ *     2 (K and V) * layers * batch * kv_heads * seq * head_dim * dtype_bytes
+ * ("KV cache complete guide" (techblog.paldyn.com), section "KV cache memory
+ * size calculation"; "Transformer attention mask and KV cache inference",
+ * section "Cache shape and memory calculation").  Returns -1 if any argument
+ * is negative or the product overflows int64. */
+int64_t kv_bytes(int layers, int batch, int kv_heads, int64_t seq, int head_dim, int dtype_bytes);
+
+/* --------------------------------------------------- host block allocator */
+
+/* Library-owned host object: a pool of num_blocks 16-token blocks with a
+ * free list and per-block reference counts, plus the sequences that own
+ * blocks ("KV Cache, Flash Attention and inference optimization", section
+ * "PagedAttention" and exercise 3: fixed 16-token blocks, a free list, blocks
+ * returned to the pool when a sequence ends; "KV cache complete guide",
+ * section "(4) PagedAttention": requests with a common prefix share physical
+ * blocks, copy-on-write).  Not thread-safe: one caller thread at a time. */
+typedef struct kv_alloc kv_alloc_t;
+
+/* Create an allocator.  block_size must be 16; num_kv_heads, head_dim and
+ * kv_dtype are recorded for kv_alloc_stats and checks.  *out receives the
+ * handle (NULL on failure).  The caller allocates the device caches itself
+ * ([num_blocks][num_kv_heads][16][head_dim] per layer, K and V). */
+int kv_cache_alloc(kv_alloc_t** out, int num_blocks, int num_kv_heads, int head_dim,
+                   int block_size, int kv_dtype);
+
+/* Destroy an allocator (NULL is ignored). */
+void kv_alloc_destroy(kv_alloc_t* a);
+
+/* Register sequence seq_id holding `len` prefilled tokens: takes
+ * ceil(len/16) blocks from the free list.  KV_ERR_EXISTS if the id is in use,
+ * KV_ERR_OUT_OF_BLOCKS (and no change) if the pool is too small. */
+int kv_seq_add(kv_alloc_t* a, int64_t seq_id, int64_t len);
+
+/* New sequence `child` that shares the first ceil(shared_len/16) blocks of
+ * `parent` (reference counts incremented, no copy) and has length
+ * shared_len <= len(parent).  A later append into a shared partial block
+ * copies it first (see kv_step).  Beam/parallel-sample branching and
+ * common-prefix reuse both use this. */
+int kv_seq_fork(kv_alloc_t* a, int64_t parent, int64_t child, int64_t shared_len);
+
+/* End a sequence: drop one reference from each of its blocks; blocks that
+ * reach zero return to the free list.  KV_ERR_NOT_FOUND for unknown ids. */
+int kv_seq_free(kv_alloc_t* a, int64_t seq_id);
+
+/* Plan one decode step for n sequences (the append contract of
+ * "Transformer attention mask and KV cache inference", section "Position ID
+ * and append contract": the new token goes at position == current length).
+ * For row i (sequence seq_ids[i], current length pos):
+ *   - if pos % 16 == 0 a fresh block is taken from the free list;
+ *   - else if the tail block is shared (refcount > 1) a fresh block is taken,
+ *     the pair (old, new) is reported in cow_src/cow_dst so the caller can
+ *     copy its contents on the GPU (kv_copy_blocks) before appending, and the
+ *     old block loses one reference;
+ *   - slot_mapping[i] = block_table[pos / 16] * 16 + pos % 16;
+ *   - the sequence length becomes pos + 1 and context_lens[i] = pos + 1;
+ *   - block_tables[i*max_blocks ...] receives the sequence's block ids, the
+ *     rest of the row is filled with -1.
+ * All outputs are host arrays: slot_mapping[n] int64, block_tables
+ * [n][max_blocks] int32, context_lens[n] int32, cow_src/cow_dst[cow_cap]
+ * int32, *n_cow.  The step is all-or-nothing: on KV_ERR_OUT_OF_BLOCKS,
+ * KV_ERR_NOT_FOUND, a repeated id, a row longer than max_blocks or
+ * cow_cap < needed copies (KV_ERR_INVALID_ARG) nothing changes. */
+int kv_step(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* slot_mapping,
+            int32_t* block_tables, int max_blocks, int32_t* context_lens, int32_t* cow_src,
+            int32_t* cow_dst, int cow_cap, int* n_cow);
+
+/* Read a sequence's state: *len (may be NULL), and its block ids into
+ * row[max_blocks] (may be NULL; -1 padded).  *nblocks (may be NULL) gets
+ * the number of blocks it holds.  KV_ERR_INVALID_ARG if row is too short. */
+int kv_seq_info(kv_alloc_t* a, int64_t seq_id, int64_t* len, int32_t* row, int max_blocks,
+                int* nblocks);
+
+/* Pool statistics: free blocks, blocks in use, live sequences, and the
+ * reference count of one block (block < 0: skipped). */
+int kv_alloc_stats(kv_alloc_t* a, int* free_blocks, int* used_blocks, int* num_seqs,
+                   int block, int* refcount);
+
+/* Slot of position positions[i] of sequence row i of block_tables (host):
+ *     slot = block_tables[i][pos / 16] * 16 + pos % 16
+ * ("KV Cache, Flash Attention and inference optimization", section
+ * "PagedAttention": the page table maps a logical position to a physical
+ * block).  A negative position gives slot -1 (a padding token).
+ * KV_ERR_INVALID_ARG if pos / 16 >= max_blocks or the entry is negative. */
+int kv_slot_mapping(const int32_t* block_tables, int max_blocks, const int64_t* positions,
+                    int n, int64_t* slot_mapping);
+
+/* ------------------------------------------------------------- GPU: append */
+
+/* Write each token's K and V into its cache slot (device pointers):
+ *   k, v:          [num_tokens][num_kv_heads][head_dim] bfloat16
+ *   slot_mapping:  [num_tokens] int64, slot = block * 16 + offset; a slot < 0
+ *                  skips the token (padding); a slot >= num_blocks*16 is
+ *                  skipped and flags KV_DEVERR_SLOT_OUT_OF_RANGE
+ *   k_cache, v_cache: the layer's caches (layout above)
+ *   kv_dtype:      KV_DTYPE_BF16 (bit copy) or KV_DTYPE_FP8_E4M3: code =
+ *                  E4M3(x / scale), quotient in binary32, round to nearest
+ *                  even, saturating to +-448 ("KV cache complete guide",
+ *                  section "(1) FP8 quantization": an FP8 KV cache halves its
+ *                  memory).  k_scale / v_scale must be finite and > 0.
+ * Tokens with equal slots race (last writer wins, unspecified). */
+int kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
+              const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+              int num_blocks, int kv_dtype, float k_scale, float v_scale, void* stream);
+
+/* Copy whole blocks (all KV heads, K and V) src[i] -> dst[i] inside the
+ * caches; src/dst are device int32 arrays of n ids.  Used for the
+ * copy-on-write pairs reported by kv_step ("KV cache complete guide",
+ * section "(4) PagedAttention": shared blocks are copy-on-write).  Ids
+ * outside [0, num_blocks) are skipped and flag KV_DEVERR_BLOCK_OUT_OF_RANGE.
+ * A dst that is also some src in the same call gives an unspecified result. */
+int kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int n,
+                   int num_kv_heads, int head_dim, int num_blocks, int kv_dtype, void* stream);
+
+/* --------------------------------------------------- GPU: decode attention */
+
+/* Workspace bytes paged_decode_attention needs on the current device for
+ * this shape (split-KV partial outputs, their log-sum-exp terms and a small
+ * per-(sequence, KV head) table).  Queries the device; KV_ERR_CUDA without
+ * one.  The workspace needs no initialisation and carries nothing from one
+ * call to the next; calls that overlap on the GPU need separate workspaces. */
+int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int kv_dtype, size_t* bytes);
+
+/* One decode step of attention over a paged cache (all device pointers):
+ *   out:           [num_seqs][num_q_heads][head_dim], out_dtype KV_DTYPE_BF16
+ *                  (rounded to nearest even) or KV_DTYPE_F32
+ *   q:             [num_seqs][num_q_heads][head_dim] bfloat16
+ *   k_cache, v_cache: layout above, kv_dtype; fp8 values are code * k_scale
+ *                  (K) and code * v_scale (V).  Base addresses 16-byte aligned.
+ *   num_blocks:    blocks in the pool (block ids must lie in [0, num_blocks))
+ *   block_tables:  [num_seqs][max_blocks_per_seq] int32; only the first
+ *                  ceil(context_lens[s]/16) entries of row s are read
+ *   context_lens:  [num_seqs] int32, the number of cached tokens each query
+ *                  attends over (after this step's append)
+ *   scale:         the softmax scale, normally 1/sqrt(head_dim)
+ *   workspace:     device buffer of paged_decode_workspace_bytes(...) bytes,
+ *                  16-byte aligned
+ * Computes, for query head h of sequence s and KV head hk = h / G,
+ *     out[s][h] = sum_j softmax_j(scale * q[s][h] . K[s][hk][j]) V[s][hk][j]
+ * over key positions j < context_lens[s] (the length mask of "Transformer
+ * attention mask and KV cache inference", section "Padding mask and batch
+ * length"; the formula of "KV Cache" (heepie), section "Self-Attention").
+ * The softmax runs as an online (running max, running sum) pass over 16-token
+ * blocks, split across warps and merged with the log-sum-exp rule ("KV Cache,
+ * Flash Attention and inference optimization", section "Numerical trick":
+ * the running (max, sum) makes the tiled result exact).  A sequence with
+ * context_lens[s] == 0 gets zeros.  Deterministic: the same inputs on the
+ * same device give bit-identical outputs, whatever the physical block ids. */
+int paged_decode_attention(void* out, int out_dtype, const void* q, const void* k_cache,
+                           const void* v_cache, int kv_dtype, float k_scale, float v_scale,
+                           int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* The same operation, recording caller-created CUDA events (cudaEvent_t
+ * passed as void*, each may be NULL) on `stream` immediately before the
+ * split-KV kernel, after it, and after the merge kernel, so that a caller can
+ * time the library's own launches on the stream they run on.  This is a
+ * measurement hook of this implementation (the pages have no counterpart). */
+int paged_decode_attention_timed(void* out, int out_dtype, const void* q, const void* k_cache,
+                                 const void* v_cache, int kv_dtype, float k_scale, float v_scale,
+                                 int num_blocks, const int32_t* block_tables,
+                                 int max_blocks_per_seq, const int32_t* context_lens,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 void* stream, void* ev_split_begin, void* ev_split_end,
+                                 void* ev_combine_end);
+
+/* ------------------------------------------------------------- diagnostics */
+
+/* Read (synchronously, on the current device) and clear the sticky device
+ * error flags (KV_DEVERR_* bits) set by the kernels' bounds checks; *detail
+ * receives the first offending value (slot, block id or length), or -1. */
+int kv_get_device_error(int* flags, int64_t* detail);
+
+/* Library version string, e.g. "pagedkv 0.1 sm_103a". */
+const char* kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H */

@@ -1,0 +1,296 @@
+"""Thin Python binding of libpagedkv, the GB300 paged KV-cache decode library.
+
+Argument marshalling only: every step of the decode path (slot mapping,
+append, attention, split merge) runs in the native library declared in
+``include/paged_kv.h``.  Importing this package without the built library
+raises ``ImportError``; there is no fallback.
+
+Typical decode step for one layer::
+
+    alloc = BlockAllocator(num_blocks, kv_heads, head_dim)
+    slots, tables, lens, cow = alloc.step(seq_ids, max_blocks)      # host
+    kv_copy_blocks(k_cache, v_cache, cow_src, cow_dst)              # if any copy-on-write
+    kv_append(k_new, v_new, k_cache, v_cache, slots_dev)            # GPU
+    paged_decode_attention(out, q, k_cache, v_cache, tables_dev, lens_dev, scale, ws)  # GPU
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB as _LIB_PATH
+
+KV_OK = 0
+KV_ERR_INVALID_ARG = -1
+KV_ERR_OUT_OF_BLOCKS = -2
+KV_ERR_UNSUPPORTED = -3
+KV_ERR_CUDA = -4
+KV_ERR_NOT_FOUND = -5
+KV_ERR_EXISTS = -6
+
+BF16 = 0
+FP8_E4M3 = 1
+F32 = 2
+BLOCK_SIZE = 16
+
+DEVERR_SLOT_OUT_OF_RANGE = 1
+DEVERR_BLOCK_OUT_OF_RANGE = 2
+DEVERR_CONTEXT_TOO_LONG = 4
+DEVERR_PIPELINE_TIMEOUT = 8
+
+_ERRNAMES = {KV_ERR_INVALID_ARG: "KV_ERR_INVALID_ARG", KV_ERR_OUT_OF_BLOCKS: "KV_ERR_OUT_OF_BLOCKS",
+             KV_ERR_UNSUPPORTED: "KV_ERR_UNSUPPORTED", KV_ERR_CUDA: "KV_ERR_CUDA",
+             KV_ERR_NOT_FOUND: "KV_ERR_NOT_FOUND", KV_ERR_EXISTS: "KV_ERR_EXISTS"}
+
+
+class KVError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__("%s failed: %s (%d)" % (what, _ERRNAMES.get(code, "?"), code))
+        self.code = code
+
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError("libpagedkv.so is not built (expected at %s); run "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`" % _LIB_PATH)
+
+_lib = ctypes.CDLL(_LIB_PATH)
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+
+# exported entry points with their C signatures (include/paged_kv.h)
+_SIGS = {
+    "kv_bytes": (_i64, [_i, _i, _i, _i64, _i, _i]),
+    "kv_cache_alloc": (_i, [ctypes.POINTER(_p), _i, _i, _i, _i, _i]),
+    "kv_alloc_destroy": (None, [_p]),
+    "kv_seq_add": (_i, [_p, _i64, _i64]),
+    "kv_seq_fork": (_i, [_p, _i64, _i64, _i64]),
+    "kv_seq_free": (_i, [_p, _i64]),
+    "kv_step": (_i, [_p, _p, _i, _p, _p, _i, _p, _p, _p, _i, ctypes.POINTER(_i)]),
+    "kv_seq_info": (_i, [_p, _i64, ctypes.POINTER(_i64), _p, _i, ctypes.POINTER(_i)]),
+    "kv_alloc_stats": (_i, [_p, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i), _i,
+                            ctypes.POINTER(_i)]),
+    "kv_slot_mapping": (_i, [_p, _i, _p, _i, _p]),
+    "kv_append": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _f, _f, _p]),
+    "kv_copy_blocks": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p]),
+    "paged_decode_workspace_bytes": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]),
+    "paged_decode_attention": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i, _i,
+                                    _i, _f, _p, ctypes.c_size_t, _p]),
+    "paged_decode_attention_timed": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
+                                          _i, _i, _i, _f, _p, ctypes.c_size_t, _p, _p, _p, _p]),
+    "kv_get_device_error": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_i64)]),
+    "kv_version": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def native_library_path():
+    return _LIB_PATH
+
+
+def version():
+    return _lib.kv_version().decode()
+
+
+def _check(rc, what):
+    if rc != KV_OK:
+        raise KVError(rc, what)
+
+
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _dptr(t):
+    """Device (or host) address of a torch tensor."""
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cache_dtype(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return FP8_E4M3
+    raise ValueError("cache tensors must be bfloat16 or uint8 (E4M3 codes)")
+
+
+# ------------------------------------------------------------------ sizing
+
+def kv_bytes(layers, batch, kv_heads, seq, head_dim, dtype_bytes):
+    """2 x layers x batch x kv_heads x seq x head_dim x dtype_bytes (int)."""
+    r = _lib.kv_bytes(layers, batch, kv_heads, seq, head_dim, dtype_bytes)
+    if r < 0:
+        raise ValueError("kv_bytes: negative argument or overflow")
+    return r
+
+
+def slot_mapping(block_tables, positions):
+    """Host slot of positions[i] in block-table row i (numpy int32 [n, max_blocks])."""
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    n = pos.shape[0]
+    assert bt.shape[0] == n
+    out = np.empty(n, dtype=np.int64)
+    _check(_lib.kv_slot_mapping(_np_ptr(bt), bt.shape[1], _np_ptr(pos), n, _np_ptr(out)),
+           "kv_slot_mapping")
+    return out
+
+
+# ---------------------------------------------------------------- allocator
+
+class BlockAllocator:
+    """Host block pool with free list, reference counts and copy-on-write."""
+
+    def __init__(self, num_blocks, num_kv_heads, head_dim, kv_dtype=BF16):
+        h = ctypes.c_void_p()
+        _check(_lib.kv_cache_alloc(ctypes.byref(h), num_blocks, num_kv_heads, head_dim,
+                                   BLOCK_SIZE, kv_dtype), "kv_cache_alloc")
+        self._h = h
+        self.num_blocks = num_blocks
+
+    def close(self):
+        if self._h:
+            _lib.kv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, seq_id, length):
+        _check(_lib.kv_seq_add(self._h, seq_id, length), "kv_seq_add")
+
+    def fork(self, parent, child, shared_len):
+        _check(_lib.kv_seq_fork(self._h, parent, child, shared_len), "kv_seq_fork")
+
+    def free(self, seq_id):
+        _check(_lib.kv_seq_free(self._h, seq_id), "kv_seq_free")
+
+    def step(self, seq_ids, max_blocks, cow_cap=None):
+        """Plan one decode step; returns (slot_mapping int64[n], block_tables
+        int32[n, max_blocks], context_lens int32[n], (cow_src, cow_dst))."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        cap = n if cow_cap is None else cow_cap
+        slots = np.empty(n, dtype=np.int64)
+        bt = np.empty((n, max_blocks), dtype=np.int32)
+        lens = np.empty(n, dtype=np.int32)
+        src = np.empty(max(cap, 1), dtype=np.int32)
+        dst = np.empty(max(cap, 1), dtype=np.int32)
+        ncow = _i(0)
+        _check(_lib.kv_step(self._h, _np_ptr(ids), n, _np_ptr(slots), _np_ptr(bt), max_blocks,
+                            _np_ptr(lens), _np_ptr(src), _np_ptr(dst), cap, ctypes.byref(ncow)),
+               "kv_step")
+        return slots, bt, lens, (src[:ncow.value].copy(), dst[:ncow.value].copy())
+
+    def info(self, seq_id, max_blocks=None):
+        """(length, block ids) of a sequence."""
+        ln = _i64(0)
+        nb = _i(0)
+        _check(_lib.kv_seq_info(self._h, seq_id, ctypes.byref(ln), None, 0, ctypes.byref(nb)),
+               "kv_seq_info")
+        row = np.empty(max(nb.value, 1), dtype=np.int32)
+        _check(_lib.kv_seq_info(self._h, seq_id, None, _np_ptr(row), row.shape[0], None),
+               "kv_seq_info")
+        return ln.value, row[:nb.value].copy()
+
+    def stats(self, block=-1):
+        """(free blocks, used blocks, live sequences, refcount of `block` or None)."""
+        fb, ub, ns, rc = _i(0), _i(0), _i(0), _i(0)
+        _check(_lib.kv_alloc_stats(self._h, ctypes.byref(fb), ctypes.byref(ub), ctypes.byref(ns),
+                                   block, ctypes.byref(rc)), "kv_alloc_stats")
+        return fb.value, ub.value, ns.value, (rc.value if block >= 0 else None)
+
+
+# -------------------------------------------------------------------- GPU ops
+
+def kv_append(k, v, k_cache, v_cache, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):
+    """Append K/V ([T, Hkv, D] bfloat16, device) at slot_mapping (int64 [T],
+    device) into the caches ([NB, Hkv, 16, D], bfloat16 or uint8 E4M3)."""
+    T, Hkv, D = k.shape
+    NB = k_cache.shape[0]
+    _check(_lib.kv_append(_dptr(k), _dptr(v), _dptr(k_cache), _dptr(v_cache),
+                          _dptr(slot_mapping), T, Hkv, D, NB, _cache_dtype(k_cache),
+                          float(k_scale), float(v_scale), _stream_ptr(stream)), "kv_append")
+
+
+def kv_copy_blocks(k_cache, v_cache, src, dst, stream=None):
+    """Copy whole blocks src[i] -> dst[i] (device int32 tensors)."""
+    NB, Hkv, _, D = k_cache.shape
+    _check(_lib.kv_copy_blocks(_dptr(k_cache), _dptr(v_cache), _dptr(src), _dptr(dst),
+                               src.shape[0], Hkv, D, NB, _cache_dtype(k_cache),
+                               _stream_ptr(stream)), "kv_copy_blocks")
+
+
+def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=BF16):
+    n = ctypes.c_size_t(0)
+    _check(_lib.paged_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             kv_dtype, ctypes.byref(n)),
+           "paged_decode_workspace_bytes")
+    return n.value
+
+
+def alloc_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype=BF16, device=None):
+    import torch
+    nbytes = workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale, workspace,
+                           k_scale=1.0, v_scale=1.0, stream=None):
+    """out[B, Hq, D] (bfloat16 or float32) = decode attention of q [B, Hq, D]
+    (bfloat16) over the paged caches; block_tables int32 [B, max_blocks] and
+    context_lens int32 [B] on the device; workspace a uint8 device tensor of
+    at least workspace_bytes(...) bytes."""
+    import torch
+    B, Hq, D = q.shape
+    NB, Hkv, _, D2 = k_cache.shape
+    assert D == D2
+    out_dtype = F32 if out.dtype == torch.float32 else BF16
+    _check(_lib.paged_decode_attention(
+        _dptr(out), out_dtype, _dptr(q), _dptr(k_cache), _dptr(v_cache), _cache_dtype(k_cache),
+        float(k_scale), float(v_scale), NB, _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), B, Hq, Hkv, D, float(scale), _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+        "paged_decode_attention")
+
+
+def paged_decode_attention_timed(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                 workspace, events, k_scale=1.0, v_scale=1.0, stream=None):
+    """paged_decode_attention that also records three torch.cuda.Event objects
+    (already recorded once, so that their handles exist) around the split and
+    merge launches: events = (before split, after split, after merge)."""
+    import torch
+    B, Hq, D = q.shape
+    NB, Hkv, _, _ = k_cache.shape
+    out_dtype = F32 if out.dtype == torch.float32 else BF16
+    ev = [ctypes.c_void_p(e._as_parameter_.value if hasattr(e._as_parameter_, "value")
+                          else e._as_parameter_) for e in events]
+    _check(_lib.paged_decode_attention_timed(
+        _dptr(out), out_dtype, _dptr(q), _dptr(k_cache), _dptr(v_cache), _cache_dtype(k_cache),
+        float(k_scale), float(v_scale), NB, _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), B, Hq, Hkv, D, float(scale), _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream), ev[0], ev[1], ev[2]),
+        "paged_decode_attention_timed")
+
+
+def get_device_error():
+    """(flags, detail) of the kernels' sticky bounds-check flags; clears them."""
+    f = _i(0)
+    d = _i64(0)
+    _check(_lib.kv_get_device_error(ctypes.byref(f), ctypes.byref(d)), "kv_get_device_error")
+    return f.value, d.value

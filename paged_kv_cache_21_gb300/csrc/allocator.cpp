@@ -1,0 +1,252 @@
+// Host side of the paged KV cache: KV sizing, the block allocator with its free
+// list and reference counts, and the per-step slot mapping.
+//
+// "KV Cache, Flash Attention and inference optimization", section
+// "PagedAttention" (16-token blocks, a page table from logical position to
+// physical block) and its exercise 3 (a free list; blocks go back to the pool
+// when a sequence ends); "KV cache complete guide", section "(4)
+// PagedAttention" (requests with a common prefix share physical blocks,
+// copy-on-write); "Transformer attention mask and KV cache inference",
+// section "Position ID and append contract" (a cache handle owns its length;
+// the new token goes at position == current length).
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "paged_kv.h"
+
+namespace {
+
+struct Seq {
+    int64_t len = 0;
+    std::vector<int32_t> blocks;
+};
+
+int64_t ceil_blocks(int64_t len) { return (len + KV_BLOCK_SIZE - 1) / KV_BLOCK_SIZE; }
+
+}  // namespace
+
+struct kv_alloc {
+    int num_blocks = 0;
+    int num_kv_heads = 0;
+    int head_dim = 0;
+    int kv_dtype = 0;
+    std::vector<int32_t> free_list;   // stack; the next block handed out is back()
+    std::vector<int32_t> refcount;    // per physical block
+    std::unordered_map<int64_t, Seq> seqs;
+
+    int32_t take() {
+        int32_t b = free_list.back();
+        free_list.pop_back();
+        refcount[b] = 1;
+        return b;
+    }
+    void release(int32_t b) {
+        if (--refcount[b] == 0) free_list.push_back(b);
+    }
+};
+
+extern "C" {
+
+int64_t kv_bytes(int layers, int batch, int kv_heads, int64_t seq, int head_dim, int dtype_bytes)
+{
+    if (layers < 0 || batch < 0 || kv_heads < 0 || seq < 0 || head_dim < 0 || dtype_bytes < 0)
+        return -1;
+    int64_t r = 2;
+    const int64_t f[6] = {layers, batch, kv_heads, seq, head_dim, dtype_bytes};
+    for (int64_t x : f)
+        if (__builtin_mul_overflow(r, x, &r)) return -1;
+    return r;
+}
+
+int kv_cache_alloc(kv_alloc_t** out, int num_blocks, int num_kv_heads, int head_dim,
+                   int block_size, int kv_dtype)
+{
+    if (!out) return KV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0) return KV_ERR_INVALID_ARG;
+    if (block_size != KV_BLOCK_SIZE) return KV_ERR_UNSUPPORTED;
+    if (kv_dtype != KV_DTYPE_BF16 && kv_dtype != KV_DTYPE_FP8_E4M3) return KV_ERR_UNSUPPORTED;
+    kv_alloc* a = new (std::nothrow) kv_alloc;
+    if (!a) return KV_ERR_INVALID_ARG;
+    a->num_blocks = num_blocks;
+    a->num_kv_heads = num_kv_heads;
+    a->head_dim = head_dim;
+    a->kv_dtype = kv_dtype;
+    a->refcount.assign(num_blocks, 0);
+    a->free_list.resize(num_blocks);
+    // hand out 0, 1, 2, ... first
+    for (int i = 0; i < num_blocks; ++i) a->free_list[i] = num_blocks - 1 - i;
+    *out = a;
+    return KV_OK;
+}
+
+void kv_alloc_destroy(kv_alloc_t* a) { delete a; }
+
+int kv_seq_add(kv_alloc_t* a, int64_t seq_id, int64_t len)
+{
+    if (!a || len < 0) return KV_ERR_INVALID_ARG;
+    if (a->seqs.count(seq_id)) return KV_ERR_EXISTS;
+    int64_t need = ceil_blocks(len);
+    if (need > (int64_t)a->free_list.size()) return KV_ERR_OUT_OF_BLOCKS;
+    Seq s;
+    s.len = len;
+    s.blocks.reserve(need);
+    for (int64_t i = 0; i < need; ++i) s.blocks.push_back(a->take());
+    a->seqs.emplace(seq_id, std::move(s));
+    return KV_OK;
+}
+
+int kv_seq_fork(kv_alloc_t* a, int64_t parent, int64_t child, int64_t shared_len)
+{
+    if (!a || shared_len < 0) return KV_ERR_INVALID_ARG;
+    auto it = a->seqs.find(parent);
+    if (it == a->seqs.end()) return KV_ERR_NOT_FOUND;
+    if (a->seqs.count(child)) return KV_ERR_EXISTS;
+    if (shared_len > it->second.len) return KV_ERR_INVALID_ARG;
+    Seq s;
+    s.len = shared_len;
+    int64_t nshare = ceil_blocks(shared_len);
+    s.blocks.assign(it->second.blocks.begin(), it->second.blocks.begin() + nshare);
+    for (int32_t b : s.blocks) a->refcount[b] += 1;
+    a->seqs.emplace(child, std::move(s));
+    return KV_OK;
+}
+
+int kv_seq_free(kv_alloc_t* a, int64_t seq_id)
+{
+    if (!a) return KV_ERR_INVALID_ARG;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return KV_ERR_NOT_FOUND;
+    for (int32_t b : it->second.blocks) a->release(b);
+    a->seqs.erase(it);
+    return KV_OK;
+}
+
+int kv_step(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* slot_mapping,
+            int32_t* block_tables, int max_blocks, int32_t* context_lens, int32_t* cow_src,
+            int32_t* cow_dst, int cow_cap, int* n_cow)
+{
+    if (!a || n < 0 || max_blocks <= 0 || cow_cap < 0) return KV_ERR_INVALID_ARG;
+    if (n > 0 && (!seq_ids || !slot_mapping || !block_tables || !context_lens))
+        return KV_ERR_INVALID_ARG;
+    if (cow_cap > 0 && (!cow_src || !cow_dst)) return KV_ERR_INVALID_ARG;
+    if (n_cow) *n_cow = 0;
+
+    // Pass 1: check everything and count the blocks the step needs, simulating
+    // the reference-count changes so that two sequences sharing a tail block
+    // are handled in order (the first copies, the second then owns it alone).
+    std::unordered_set<int64_t> seen;
+    std::unordered_map<int32_t, int> ref_delta;
+    int64_t need_new = 0, need_cow = 0;
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return KV_ERR_NOT_FOUND;
+        if (!seen.insert(seq_ids[i]).second) return KV_ERR_INVALID_ARG;
+        const Seq& s = it->second;
+        int64_t pos = s.len;
+        if (ceil_blocks(pos + 1) > max_blocks) return KV_ERR_INVALID_ARG;
+        if (pos % KV_BLOCK_SIZE == 0) {
+            need_new += 1;
+        } else {
+            int32_t tail = s.blocks[pos / KV_BLOCK_SIZE];
+            int rc = a->refcount[tail] + ref_delta[tail];
+            if (rc > 1) {
+                need_new += 1;
+                need_cow += 1;
+                ref_delta[tail] -= 1;
+            }
+        }
+    }
+    if (need_new > (int64_t)a->free_list.size()) return KV_ERR_OUT_OF_BLOCKS;
+    if (need_cow > cow_cap) return KV_ERR_INVALID_ARG;
+
+    // Pass 2: apply.
+    int ncow = 0;
+    for (int i = 0; i < n; ++i) {
+        Seq& s = a->seqs[seq_ids[i]];
+        int64_t pos = s.len;
+        int64_t bi = pos / KV_BLOCK_SIZE;
+        if (pos % KV_BLOCK_SIZE == 0) {
+            s.blocks.push_back(a->take());
+        } else {
+            int32_t tail = s.blocks[bi];
+            if (a->refcount[tail] > 1) {
+                int32_t fresh = a->take();
+                cow_src[ncow] = tail;
+                cow_dst[ncow] = fresh;
+                ++ncow;
+                a->release(tail);
+                s.blocks[bi] = fresh;
+            }
+        }
+        slot_mapping[i] = (int64_t)s.blocks[bi] * KV_BLOCK_SIZE + pos % KV_BLOCK_SIZE;
+        s.len = pos + 1;
+        context_lens[i] = (int32_t)s.len;
+        int32_t* row = block_tables + (int64_t)i * max_blocks;
+        int nb = (int)s.blocks.size();
+        std::memcpy(row, s.blocks.data(), sizeof(int32_t) * nb);
+        for (int j = nb; j < max_blocks; ++j) row[j] = -1;
+    }
+    if (n_cow) *n_cow = ncow;
+    return KV_OK;
+}
+
+int kv_seq_info(kv_alloc_t* a, int64_t seq_id, int64_t* len, int32_t* row, int max_blocks,
+                int* nblocks)
+{
+    if (!a) return KV_ERR_INVALID_ARG;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return KV_ERR_NOT_FOUND;
+    const Seq& s = it->second;
+    int nb = (int)s.blocks.size();
+    if (row) {
+        if (max_blocks < nb) return KV_ERR_INVALID_ARG;
+        std::memcpy(row, s.blocks.data(), sizeof(int32_t) * nb);
+        for (int j = nb; j < max_blocks; ++j) row[j] = -1;
+    }
+    if (len) *len = s.len;
+    if (nblocks) *nblocks = nb;
+    return KV_OK;
+}
+
+int kv_alloc_stats(kv_alloc_t* a, int* free_blocks, int* used_blocks, int* num_seqs, int block,
+                   int* refcount)
+{
+    if (!a) return KV_ERR_INVALID_ARG;
+    if (free_blocks) *free_blocks = (int)a->free_list.size();
+    if (used_blocks) *used_blocks = a->num_blocks - (int)a->free_list.size();
+    if (num_seqs) *num_seqs = (int)a->seqs.size();
+    if (block >= 0) {
+        if (block >= a->num_blocks) return KV_ERR_INVALID_ARG;
+        if (refcount) *refcount = a->refcount[block];
+    }
+    return KV_OK;
+}
+
+int kv_slot_mapping(const int32_t* block_tables, int max_blocks, const int64_t* positions, int n,
+                    int64_t* slot_mapping)
+{
+    if (n < 0 || max_blocks <= 0) return KV_ERR_INVALID_ARG;
+    if (n > 0 && (!block_tables || !positions || !slot_mapping)) return KV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        int64_t pos = positions[i];
+        if (pos < 0) {
+            slot_mapping[i] = -1;
+            continue;
+        }
+        int64_t bi = pos / KV_BLOCK_SIZE;
+        if (bi >= max_blocks) return KV_ERR_INVALID_ARG;
+        int32_t blk = block_tables[(int64_t)i * max_blocks + bi];
+        if (blk < 0) return KV_ERR_INVALID_ARG;
+        slot_mapping[i] = (int64_t)blk * KV_BLOCK_SIZE + pos % KV_BLOCK_SIZE;
+    }
+    return KV_OK;
+}
+
+const char* kv_version(void) { return "pagedkv 0.1 sm_103a"; }
+
+}  // extern "C"

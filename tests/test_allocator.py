@@ -1,0 +1,179 @@
+"""Host block allocator behind the C ABI: free list, reference counts,
+copy-on-write and the per-step slot mapping (no GPU needed)."""
+import numpy as np
+import pytest
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import __graft_entry__
+    __graft_entry__.build_native()
+    import paged_kv_cache_21_gb300 as pk
+    return pk
+
+
+def test_add_and_free_return_blocks(pk):
+    a = pk.BlockAllocator(10, 8, 128)
+    a.add(1, 33)                         # 3 blocks
+    a.add(2, 16)                         # 1 block
+    assert a.stats()[:3] == (6, 4, 2)
+    ln, row = a.info(1)
+    assert ln == 33 and len(row) == 3 and len(set(row)) == 3
+    a.free(1)
+    assert a.stats()[:3] == (9, 1, 1)
+    a.free(2)
+    assert a.stats()[:3] == (10, 0, 0)
+    with pytest.raises(pk.KVError) as e:
+        a.free(2)
+    assert e.value.code == pk.KV_ERR_NOT_FOUND
+
+
+def test_exhaustion_is_reported_and_changes_nothing(pk):
+    a = pk.BlockAllocator(4, 1, 64)
+    a.add(0, 48)                         # 3 blocks
+    with pytest.raises(pk.KVError) as e:
+        a.add(1, 17)                     # needs 2
+    assert e.value.code == pk.KV_ERR_OUT_OF_BLOCKS
+    assert a.stats()[:3] == (1, 3, 1)
+    a.add(1, 16)
+    # both sequences sit at a block boundary: the step needs 2 fresh blocks
+    with pytest.raises(pk.KVError) as e:
+        a.step([0, 1], 8)
+    assert e.value.code == pk.KV_ERR_OUT_OF_BLOCKS
+    assert a.info(0)[0] == 48 and a.info(1)[0] == 16
+    with pytest.raises(pk.KVError) as e:
+        a.add(0, 1)
+    assert e.value.code == pk.KV_ERR_EXISTS
+
+
+def test_step_slot_mapping_and_block_growth(pk):
+    a = pk.BlockAllocator(64, 2, 64)
+    a.add(7, 0)
+    a.add(9, 15)
+    for step in range(40):
+        slots, bt, lens, (cs, cd) = a.step([7, 9], 6)
+        assert len(cs) == 0
+        assert list(lens) == [step + 1, step + 16]
+        # the new token goes at position == previous length
+        want = oracle.slot_mapping(bt, np.arange(2), lens.astype(np.int64) - 1)
+        np.testing.assert_array_equal(slots, want)
+        for i in range(2):
+            nb = -(-int(lens[i]) // 16)
+            assert np.all(bt[i, :nb] >= 0) and np.all(bt[i, nb:] == -1)
+    # a row too short for the next append is refused, nothing changes
+    with pytest.raises(pk.KVError):
+        a.step([9], 3)
+    assert a.info(9)[0] == 55
+
+
+def test_fork_shares_blocks_and_copies_on_write(pk):
+    a = pk.BlockAllocator(32, 4, 128)
+    a.add(0, 40)                                 # blocks b0 b1 b2, b2 partial (8 tokens)
+    _, row0 = a.info(0)
+    a.fork(0, 1, 40)
+    a.fork(0, 2, 40)
+    for b in row0:
+        assert a.stats(int(b))[3] == 3
+    assert a.stats()[1] == 3                     # no new blocks used by forking
+    slots, bt, lens, (cs, cd) = a.step([0, 1, 2], 8)
+    # the first two appenders find the shared partial tail and copy it; the
+    # third is then its only owner and appends in place
+    assert list(cs) == [row0[2], row0[2]]
+    assert len(set(cd)) == 2 and row0[2] not in cd
+    assert bt[2, 2] == row0[2]
+    assert bt[0, 2] == cd[0] and bt[1, 2] == cd[1]
+    assert a.stats(int(row0[2]))[3] == 1
+    for b in row0[:2]:
+        assert a.stats(int(b))[3] == 3           # full prefix blocks stay shared
+    np.testing.assert_array_equal(slots, oracle.slot_mapping(bt, np.arange(3), [40, 40, 40]))
+    a.free(0)
+    a.free(1)
+    a.free(2)
+    assert a.stats()[:3] == (32, 0, 0)
+
+
+def test_fork_at_block_boundary_needs_no_copy(pk):
+    a = pk.BlockAllocator(16, 1, 64)
+    a.add(0, 32)
+    a.fork(0, 1, 32)
+    slots, bt, lens, (cs, cd) = a.step([0, 1], 4)
+    assert len(cs) == 0
+    assert bt[0, 2] != bt[1, 2]
+    assert bt[0, 0] == bt[1, 0] and bt[0, 1] == bt[1, 1]
+
+
+def test_fork_of_a_prefix_shorter_than_parent(pk):
+    a = pk.BlockAllocator(16, 1, 64)
+    a.add(0, 50)
+    a.fork(0, 1, 20)                             # shares b0 and the partial b1
+    assert a.info(1)[0] == 20 and len(a.info(1)[1]) == 2
+    slots, bt, lens, (cs, cd) = a.step([1], 4)
+    assert list(cs) == [a.info(0)[1][1]]         # b1 is shared and partial for seq 1
+    with pytest.raises(pk.KVError):
+        a.fork(0, 2, 51)                         # longer than the parent
+
+
+def test_step_rejects_bad_requests_atomically(pk):
+    a = pk.BlockAllocator(16, 1, 64)
+    a.add(0, 5)
+    a.add(1, 5)
+    before = (a.info(0), a.info(1), a.stats())
+    for ids in ([0, 99], [0, 0]):
+        with pytest.raises(pk.KVError):
+            a.step(ids, 4)
+    a.fork(0, 2, 5)
+    with pytest.raises(pk.KVError):
+        a.step([0, 2], 4, cow_cap=0)             # a copy is needed but not allowed
+    assert a.info(0)[0] == before[0][0] and a.info(1)[0] == before[1][0]
+
+
+def test_random_operations_keep_pool_invariants(pk):
+    """Model check: free + used == pool; each block's refcount equals the
+    number of live sequences holding it; every block table row matches the
+    model's view of the sequence."""
+    rng = np.random.default_rng(123)
+    NB = 200
+    a = pk.BlockAllocator(NB, 2, 64)
+    lens = {}
+    next_id = 0
+    for _ in range(1500):
+        op = rng.integers(0, 4)
+        try:
+            if op == 0:
+                ln = int(rng.integers(0, 80))
+                a.add(next_id, ln)
+                lens[next_id] = ln
+                next_id += 1
+            elif op == 1 and lens:
+                sid = int(rng.choice(list(lens)))
+                a.free(sid)
+                del lens[sid]
+            elif op == 2 and lens:
+                sid = int(rng.choice(list(lens)))
+                sl = int(rng.integers(0, lens[sid] + 1))
+                a.fork(sid, next_id, sl)
+                lens[next_id] = sl
+                next_id += 1
+            elif op == 3 and lens:
+                ids = rng.choice(list(lens), size=min(len(lens), 5), replace=False)
+                slots, bt, ln, _ = a.step(ids, 64)
+                for i, sid in enumerate(ids):
+                    lens[int(sid)] += 1
+                    assert ln[i] == lens[int(sid)]
+                np.testing.assert_array_equal(
+                    slots, oracle.slot_mapping(bt, np.arange(len(ids)), ln.astype(np.int64) - 1))
+        except pk.KVError as e:
+            assert e.code in (pk.KV_ERR_OUT_OF_BLOCKS, pk.KV_ERR_INVALID_ARG)
+        free, used, nseq, _ = a.stats()
+        assert free + used == NB and nseq == len(lens)
+    holders = {}
+    for sid, ln in lens.items():
+        got_len, row = a.info(sid)
+        assert got_len == ln and len(row) == -(-ln // 16)
+        for b in row:
+            holders[int(b)] = holders.get(int(b), 0) + 1
+    for b in range(NB):
+        assert a.stats(b)[3] == holders.get(b, 0)
+    assert a.stats()[1] == len(holders)

@@ -1,0 +1,323 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Append and block indexing must be bit-exact; attention
+outputs must be within 2e-3 (bfloat16 KV) or 3e-2 (E4M3 KV) of the float64
+oracle, plus half a bfloat16 ulp when the output itself is bfloat16."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from workloads import bf16_bits
+
+import decode_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_21_gb300 as pk  # noqa: F401  (fails loudly without the library)
+    torch.cuda.set_device(0)
+    yield
+    import paged_kv_cache_21_gb300 as pk
+    flags, detail = pk.get_device_error()
+    assert flags == 0, "device error flags %d (detail %d) left set" % (flags, detail)
+
+
+def cache_bits(t):
+    t = t.cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def check_case(case, out_dtype=torch.bfloat16, pair_select=None, what=""):
+    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype)
+    okc, ovc = H.oracle_caches(case)
+    assert np.array_equal(cache_bits(kc), okc), "K cache differs from oracle " + what
+    assert np.array_equal(cache_bits(vc), ovc), "V cache differs from oracle " + what
+    ref = H.oracle_step(case, okc, ovc, pair_select)
+    return H.compare(case, out, ref, pair_select, what=what)
+
+
+# ---------------------------------------------------------------- append
+
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_append_bit_exact_with_padding_tokens(kv_dtype):
+    import paged_kv_cache_21_gb300 as pk
+    rng = np.random.default_rng(5)
+    NB, Hkv, D, T = 37, 4, 128, 300
+    if kv_dtype == workloads.BF16:
+        kc = torch.full((NB, Hkv, 16, D), 3.0, dtype=torch.bfloat16, device="cuda")
+    else:
+        kc = torch.full((NB, Hkv, 16, D), 0x5A, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    okc, ovc = cache_bits(kc).copy(), cache_bits(vc).copy()
+    g = torch.Generator().manual_seed(9)
+    k = (torch.randn((T, Hkv, D), generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn((T, Hkv, D), generator=g) * 0.01).to(torch.bfloat16)
+    slots = rng.permutation(NB * 16)[:T].astype(np.int64)
+    slots[::7] = -1                                         # padding tokens
+    ks, vs = float(np.float32(12.0 / 448)), float(np.float32(0.05 / 448))
+    pk.kv_append(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda(), ks, vs)
+    assert oracle.append(okc, ovc, bf16_bits(k), bf16_bits(v), slots, kv_dtype, ks, vs) == 0
+    assert np.array_equal(cache_bits(kc), okc)
+    assert np.array_equal(cache_bits(vc), ovc)
+
+
+def test_e4m3_encoder_agrees_with_hardware_conversion_on_every_bf16():
+    """All 65,536 bfloat16 patterns through kv_append (scale 1): the oracle's
+    E4M3 encoder must give the same byte as the GPU conversion (NaN inputs:
+    both NaN)."""
+    import paged_kv_cache_21_gb300 as pk
+    bits = np.arange(65536, dtype=np.uint16)
+    k = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(1, 512, 128)
+    kc = torch.zeros((1, 512, 16, 128), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    pk.kv_append(k.cuda(), k.cuda(), kc, vc, torch.zeros(1, dtype=torch.int64, device="cuda"),
+                 1.0, 1.0)
+    got = kc[0, :, 0, :].cpu().numpy().reshape(-1)
+    want = oracle.quantize_e4m3(bits, 1.0)
+    vals = oracle.bf16_bits_to_f64(bits)
+    nan_in = np.isnan(vals)
+    assert np.array_equal(got[~nan_in], want[~nan_in])
+    assert np.all((got[nan_in] & 0x7F) == 0x7F)
+
+
+def test_copy_blocks_copies_whole_blocks():
+    import paged_kv_cache_21_gb300 as pk
+    NB, Hkv, D = 9, 2, 64
+    g = torch.Generator().manual_seed(3)
+    kc = torch.randn((NB, Hkv, 16, D), generator=g).to(torch.bfloat16).cuda()
+    vc = torch.randn((NB, Hkv, 16, D), generator=g).to(torch.bfloat16).cuda()
+    k0, v0 = kc.clone(), vc.clone()
+    src = torch.tensor([1, 4, 7], dtype=torch.int32, device="cuda")
+    dst = torch.tensor([2, 0, 8], dtype=torch.int32, device="cuda")
+    pk.kv_copy_blocks(kc, vc, src, dst)
+    torch.cuda.synchronize()
+    for s, d in zip(src.tolist(), dst.tolist()):
+        assert torch.equal(kc[d], k0[s]) and torch.equal(vc[d], v0[s])
+    for b in (1, 3, 4, 5, 6, 7):
+        assert torch.equal(kc[b], k0[b]) and torch.equal(vc[b], v0[b])
+
+
+# ------------------------------------------------------------- configs
+
+@pytest.mark.parametrize("cfg,override", [
+    ("1", None),
+    ("2", {"B": 3}),                       # 3 x 8193 tokens: many splits + ragged tail
+    ("3", {"B": 24}),                      # ragged, 3 groups sharing prefix blocks
+    ("4", {"B": 1, "N": 20000}),           # G = 8, long single sequence
+    ("5a", {"B": 3}),                      # E4M3 cache
+    ("5b", {"B": 2}),                      # MHA, G = 1
+])
+def test_config_shapes_full_compare(cfg, override):
+    case = workloads.make_case(cfg, override=override)
+    err = check_case(case, what="config %s %s" % (cfg, override))
+    print("config %s %s: max abs err %.3g" % (cfg, override, err))
+
+
+@pytest.mark.parametrize("cfg,nsample", [("2", 24), ("3", 24), ("4", 8), ("5a", 24), ("5b", 24)])
+def test_config_full_size_sampled(cfg, nsample):
+    """Full-size configuration in the benchmark's launch configuration; the
+    oracle computes a seeded sample of (sequence, KV head) pairs, the caches
+    are compared in full."""
+    case = workloads.make_case(cfg)
+    sel = H.sample_pairs(case, nsample, seed=int(cfg[0]))
+    err = check_case(case, pair_select=sel, what="config %s full size" % cfg)
+    print("config %s full size: max abs err %.3g over %d pairs" % (cfg, err, int(sel.sum())))
+
+
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_float32_output_within_tolerance(kv_dtype):
+    case = workloads.make_custom(5, 32, 8, 128, [1, 17, 300, 4097, 9000], kv_dtype=kv_dtype,
+                                 seed=21)
+    err = check_case(case, out_dtype=torch.float32, what="f32 out")
+    print("f32 output max abs err %.3g" % err)
+
+
+# ------------------------------------------------------------ edge cases
+
+EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 255, 256, 257, 4095, 4096, 4097]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_edge_lengths(D, G, kv_dtype):
+    Hkv = 2
+    case = workloads.make_custom(len(EDGE_LENS), G * Hkv, Hkv, D, EDGE_LENS, kv_dtype=kv_dtype,
+                                 seed=D + G)
+    check_case(case, what="D%d G%d dt%d" % (D, G, kv_dtype))
+
+
+def test_group_sizes_two_three_five_seven():
+    for G in (2, 3, 5, 7):
+        case = workloads.make_custom(3, 3 * G, 3, 128, [40, 700, 2000], seed=G)
+        check_case(case, what="G=%d" % G)
+
+
+def test_many_sequences_beyond_register_scan():
+    # more than 256 sequences takes the second scan path of the split kernel
+    lens = (np.arange(300) * 37) % 500 + 1
+    case = workloads.make_custom(300, 8, 2, 64, lens, seed=77)
+    check_case(case, what="B=300")
+
+
+def test_empty_contexts_give_zeros():
+    lens = [0, 33, 0, 1, 0]
+    case = workloads.make_custom(5, 8, 2, 128, [max(x, 1) for x in lens], seed=4)
+    case.context_lens = np.array(lens, dtype=np.int32)
+    err = check_case(case, what="empty contexts")
+    out, _, _ = H.gpu_step(case)
+    out_np = out.float().cpu().numpy()
+    for s_, L in enumerate(lens):
+        if L == 0:
+            assert np.all(out_np[s_] == 0.0)
+    assert err < 2e-3
+
+
+def test_nan_canaries_in_unused_slots_are_never_read():
+    case = workloads.make_custom(4, 16, 4, 128, [1, 18, 333, 1000], seed=8, slack=0.5)
+    used = np.zeros(case.num_blocks * 16, dtype=bool)
+    for s, L in enumerate(case.context_lens):
+        for pos in range(int(L)):
+            used[case.block_tables[s, pos // 16] * 16 + pos % 16] = True
+    nan_bf16 = np.uint16(0x7FC0)
+
+    def poison_np(pk_bits, pv_bits):
+        pk_bits, pv_bits = pk_bits.copy(), pv_bits.copy()
+        pk_bits[~used] = nan_bf16
+        pv_bits[~used] = nan_bf16
+        return pk_bits, pv_bits
+
+    def poison_t(pk_t, pv_t):
+        m = torch.from_numpy(~used).to(pk_t.device)
+        nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device=pk_t.device)
+        return torch.where(m[:, None, None], nan, pk_t), torch.where(m[:, None, None], nan, pv_t)
+
+    out, kc, vc = H.gpu_step(case, pool_overrides=poison_t)
+    okc, ovc = H.oracle_caches(case, pool_overrides=poison_np)
+    assert np.array_equal(cache_bits(kc), okc)
+    ref = H.oracle_step(case, okc, ovc)
+    H.compare(case, out, ref, what="NaN canaries")
+
+
+def test_block_permutation_bitwise_invariant_and_deterministic():
+    """The same logical cache under two physical block layouts gives
+    bit-identical outputs, and repeated runs are bit-identical."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(6, 32, 8, 128, [5, 100, 1000, 3000, 6000, 8193], seed=12)
+    out1, kc, vc = H.gpu_step(case)
+    # relabel physical blocks with a random permutation, moving the data with them
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(case.num_blocks).astype(np.int64)
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    pt = torch.from_numpy(perm).cuda()
+    kc2[pt] = kc
+    vc2[pt] = vc
+    bt2 = np.where(case.block_tables >= 0, perm[np.maximum(case.block_tables, 0)], -1)
+    out2 = torch.empty_like(out1)
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    pk.paged_decode_attention(out2, case.q.cuda(), kc2, vc2,
+                              torch.from_numpy(bt2.astype(np.int32)).cuda(),
+                              torch.from_numpy(case.context_lens).cuda(), case.scale, ws)
+    out3 = torch.empty_like(out1)
+    pk.paged_decode_attention(out3, case.q.cuda(), kc2, vc2,
+                              torch.from_numpy(bt2.astype(np.int32)).cuda(),
+                              torch.from_numpy(case.context_lens).cuda(), case.scale, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(out2.view(torch.int16), out3.view(torch.int16))
+
+
+def test_allocator_driven_steps_with_copy_on_write():
+    """Sequences created, forked (shared prefix, copy-on-write) and stepped by
+    the host allocator; GPU copies/appends/attends; oracle replays the same
+    block tables."""
+    import paged_kv_cache_21_gb300 as pk
+    Hq, Hkv, D, NB = 8, 2, 128, 64
+    alloc = pk.BlockAllocator(NB, Hkv, D)
+    g = torch.Generator().manual_seed(31)
+    kc = torch.zeros((NB, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    okc = np.zeros((NB, Hkv, 16, D), dtype=np.uint16)
+    ovc = np.zeros_like(okc)
+    # prefill sequence 0 with 40 tokens
+    alloc.add(0, 40)
+    _, row = alloc.info(0)
+    pre_k = torch.randn((40, Hkv, D), generator=g).to(torch.bfloat16)
+    pre_v = torch.randn((40, Hkv, D), generator=g).to(torch.bfloat16)
+    bt0 = np.full((1, 8), -1, dtype=np.int32)
+    bt0[0, :len(row)] = row
+    pre_slots = np.array([row[p // 16] * 16 + p % 16 for p in range(40)], dtype=np.int64)
+    pk.kv_append(pre_k.cuda(), pre_v.cuda(), kc, vc, torch.from_numpy(pre_slots).cuda())
+    oracle.append(okc, ovc, bf16_bits(pre_k), bf16_bits(pre_v), pre_slots, oracle.BF16)
+    # two forks share the 40-token prefix (tail block 2 is partial and shared)
+    alloc.fork(0, 1, 40)
+    alloc.fork(0, 2, 40)
+    ws = pk.alloc_workspace(3, Hq, Hkv, D)
+    for step in range(20):
+        ids = [0, 1, 2]
+        slots, bt, lens, (cs, cd) = alloc.step(ids, 8)
+        if step == 0:
+            assert len(cs) == 2        # the first two appenders copy the shared tail
+        if len(cs):
+            pk.kv_copy_blocks(kc, vc, torch.from_numpy(cs).cuda(), torch.from_numpy(cd).cuda())
+            for s_, d_ in zip(cs, cd):
+                okc[d_] = okc[s_]
+                ovc[d_] = ovc[s_]
+        k = torch.randn((3, Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((3, Hkv, D), generator=g).to(torch.bfloat16)
+        q = torch.randn((3, Hq, D), generator=g).to(torch.bfloat16)
+        pk.kv_append(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda())
+        oslots = oracle.slot_mapping(bt, np.arange(3), lens.astype(np.int64) - 1)
+        assert np.array_equal(oslots, slots)
+        oracle.append(okc, ovc, bf16_bits(k), bf16_bits(v), slots, oracle.BF16)
+        out = torch.empty((3, Hq, D), dtype=torch.float32, device="cuda")
+        pk.paged_decode_attention(out, q.cuda(), kc, vc, torch.from_numpy(bt).cuda(),
+                                  torch.from_numpy(lens).cuda(), 1 / math.sqrt(D), ws)
+        ref = oracle.paged_attention(oracle.bf16_bits_to_f64(bf16_bits(q)), okc, ovc, bt, lens,
+                                     1 / math.sqrt(D))
+        torch.cuda.synchronize()
+        assert np.array_equal(cache_bits(kc), okc)
+        assert np.max(np.abs(out.cpu().numpy() - ref)) < 2e-3
+    alloc.free(1)
+    alloc.free(2)
+    alloc.free(0)
+    assert alloc.stats()[0] == NB
+
+
+def test_bad_inputs_are_flagged_not_faulted():
+    """Out-of-range slots and block ids are skipped and reported through the
+    device error word; the context stays usable."""
+    import paged_kv_cache_21_gb300 as pk
+    pk.get_device_error()
+    NB, Hkv, D = 4, 1, 64
+    kc = torch.zeros((NB, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k = torch.ones((2, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    pk.kv_append(k, k, kc, vc, torch.tensor([3, NB * 16 + 5], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    flags, detail = pk.get_device_error()
+    assert flags == pk.DEVERR_SLOT_OUT_OF_RANGE and detail == NB * 16 + 5
+    assert float(kc[0, 0, 3, 0]) == 1.0
+    out = torch.empty((1, 2, D), dtype=torch.float32, device="cuda")
+    ws = pk.alloc_workspace(1, 2, 1, D)
+    bt = torch.tensor([[0, 99]], dtype=torch.int32, device="cuda")
+    cl = torch.tensor([20], dtype=torch.int32, device="cuda")
+    pk.paged_decode_attention(out, torch.ones((1, 2, D), dtype=torch.bfloat16, device="cuda"),
+                              kc, vc, bt, cl, 0.125, ws)
+    torch.cuda.synchronize()
+    flags, detail = pk.get_device_error()
+    assert flags == pk.DEVERR_BLOCK_OUT_OF_RANGE and detail == 99
+    assert torch.isfinite(out).all()
+    # the context is still healthy
+    x = torch.ones(4, device="cuda") * 2
+    assert float(x.sum()) == 8.0
