@@ -34,7 +34,9 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": None}
+TRAFFIC = {"kernel_sha256": "33a8bf28d1f6c11e3ec12195d848e56dcccf62e87e6a1fd2174788a48455755f",
+           "bytes_per_launch": 1092060000,
+           "source": "ncu batch-8 capture scaled x4 by units (profiles/paged_decode_split_b8_full.md)"}
 
 
 def parse_args(argv=None):
@@ -51,6 +53,8 @@ def parse_args(argv=None):
                     help="CPU time budget of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (profiling a smaller case)")
     return ap.parse_args(argv)
 
 
@@ -287,7 +291,8 @@ def run_ours(args):
     import workloads
 
     cfg = args.config
-    case = workloads.make_case(cfg, device=device)
+    case = workloads.make_case(cfg, device=device,
+                               override={"B": args.batch} if args.batch else None)
     B, Hq, Hkv, D = case.B, case.Hq, case.Hkv, case.D
     NB = case.num_blocks
     cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
@@ -407,7 +412,9 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256"] == kernel_sha() else None
-    roofline = {"bound": "hbm", "kernel": "paged_decode_split_kernel<128,bf16>",
+    roofline = {"bound": "hbm",
+                "kernel": "paged_decode_split_kernel<%d,%s>" % (
+                    D, "bf16" if case.kv_dtype == workloads.BF16 else "e4m3"),
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
