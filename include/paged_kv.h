@@ -51,6 +51,7 @@ extern "C" {
 #define KV_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
 #define KV_ERR_NOT_FOUND (-5)     /* unknown sequence id */
 #define KV_ERR_EXISTS (-6)        /* sequence id already present */
+#define KV_ERR_TOO_LARGE (-7)     /* the request exceeds a fixed size limit of the library */
 
 /* --------------------------------------------------------------- data types */
 #define KV_DTYPE_BF16 0     /* bfloat16 */
@@ -236,6 +237,38 @@ int paged_decode_attention_timed(void* out, int out_dtype, const void* q, const 
                                  float scale, void* workspace, size_t workspace_bytes,
                                  void* stream, void* ev_split_begin, void* ev_split_end,
                                  void* ev_combine_end);
+
+/* Allocation-free variant of paged_decode_attention for callers that cannot
+ * allocate device memory: code running inside a host framework that owns the
+ * device memory pool and forbids its plugins to allocate, or a
+ * latency-critical path that must not call into the driver's allocator.
+ * Such a caller cannot provide the `workspace` buffer, so this entry point
+ * takes none and uses scratch that the library itself holds: a file-scope
+ * device array of KV_NOALLOC_WORKSPACE_BYTES (16 MiB) that every GPU loading
+ * the library keeps until the process exits.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.  (This is an interface of this
+ * implementation; the pages have no counterpart.)
+ *   - Arguments, layouts and results are those of paged_decode_attention
+ *     (the caller still passes every input and the output).
+ *   - A shape whose scratch (paged_decode_workspace_bytes) exceeds
+ *     KV_NOALLOC_WORKSPACE_BYTES is rejected with KV_ERR_TOO_LARGE before
+ *     anything is launched.
+ *   - The first call on each device performs a one-time set-up on that device
+ *     (it looks up the device address of the array and configures the
+ *     kernels); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents (nothing in it has to start at zero: each call rewrites
+ *     what it reads).  Calls that overlap on the GPU -- concurrent streams,
+ *     or host threads launching at once -- race on it and give undefined
+ *     results; serialise them, or use paged_decode_attention with separate
+ *     workspaces. */
+#define KV_NOALLOC_WORKSPACE_BYTES (16u << 20)
+int paged_decode_attention_noalloc(void* out, int out_dtype, const void* q, const void* k_cache,
+                                   const void* v_cache, int kv_dtype, float k_scale,
+                                   float v_scale, int num_blocks, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   float scale, void* stream);
 
 /* ------------------------------------------------------------- diagnostics */
 

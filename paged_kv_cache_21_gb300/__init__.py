@@ -27,6 +27,8 @@ KV_ERR_UNSUPPORTED = -3
 KV_ERR_CUDA = -4
 KV_ERR_NOT_FOUND = -5
 KV_ERR_EXISTS = -6
+KV_ERR_TOO_LARGE = -7
+NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 BF16 = 0
 FP8_E4M3 = 1
@@ -40,7 +42,8 @@ DEVERR_PIPELINE_TIMEOUT = 8
 
 _ERRNAMES = {KV_ERR_INVALID_ARG: "KV_ERR_INVALID_ARG", KV_ERR_OUT_OF_BLOCKS: "KV_ERR_OUT_OF_BLOCKS",
              KV_ERR_UNSUPPORTED: "KV_ERR_UNSUPPORTED", KV_ERR_CUDA: "KV_ERR_CUDA",
-             KV_ERR_NOT_FOUND: "KV_ERR_NOT_FOUND", KV_ERR_EXISTS: "KV_ERR_EXISTS"}
+             KV_ERR_NOT_FOUND: "KV_ERR_NOT_FOUND", KV_ERR_EXISTS: "KV_ERR_EXISTS",
+             KV_ERR_TOO_LARGE: "KV_ERR_TOO_LARGE"}
 
 
 class KVError(RuntimeError):
@@ -79,6 +82,8 @@ _SIGS = {
                                     _i, _f, _p, ctypes.c_size_t, _p]),
     "paged_decode_attention_timed": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
                                           _i, _i, _i, _f, _p, ctypes.c_size_t, _p, _p, _p, _p]),
+    "paged_decode_attention_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
+                                            _i, _i, _i, _f, _p]),
     "kv_get_device_error": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_i64)]),
     "kv_version": (ctypes.c_char_p, []),
 }
@@ -286,6 +291,23 @@ def paged_decode_attention_timed(out, q, k_cache, v_cache, block_tables, context
         _dptr(context_lens), B, Hq, Hkv, D, float(scale), _dptr(workspace),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream), ev[0], ev[1], ev[2]),
         "paged_decode_attention_timed")
+
+
+def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   k_scale=1.0, v_scale=1.0, stream=None):
+    """paged_decode_attention without a caller workspace, for callers that
+    cannot allocate device memory: the library's own fixed 16 MiB scratch is
+    used (shared by every call on the device, so calls must not overlap on
+    the GPU).  Shapes needing more raise KVError(KV_ERR_TOO_LARGE)."""
+    import torch
+    B, Hq, D = q.shape
+    NB, Hkv, _, _ = k_cache.shape
+    out_dtype = F32 if out.dtype == torch.float32 else BF16
+    _check(_lib.paged_decode_attention_noalloc(
+        _dptr(out), out_dtype, _dptr(q), _dptr(k_cache), _dptr(v_cache), _cache_dtype(k_cache),
+        float(k_scale), float(v_scale), NB, _dptr(block_tables), block_tables.shape[1],
+        _dptr(context_lens), B, Hq, Hkv, D, float(scale), _stream_ptr(stream)),
+        "paged_decode_attention_noalloc")
 
 
 def get_device_error():

@@ -827,6 +827,35 @@ int decode_read_error(unsigned* flags, long long* detail)
     return KV_OK;
 }
 
+// ------------------------------------------------- fixed, library-owned scratch
+// Scratch of the allocation-free entry point: a file-scope device array that
+// every device loading the library holds until the process exits.  Host code
+// must not use the symbol's name as an address: its device address is looked
+// up once per device with cudaGetSymbolAddress (with that device current).
+constexpr size_t kStaticWorkspaceBytes = 16u << 20;     // 16 MiB
+__device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
+
+namespace {
+
+void* g_static_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_static_workspace on the current device (set up once).
+int static_workspace(void** ptr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_static_ws_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return KV_ERR_CUDA;
+        g_static_ws_ptr[dev] = p;
+    }
+    *ptr = g_static_ws_ptr[dev];
+    return KV_OK;
+}
+
+}  // namespace
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -959,4 +988,28 @@ extern "C" int kv_get_device_error(int* flags, int64_t* detail)
     if (flags) *flags = (int)(f1 | f2);
     if (detail) *detail = f1 ? d1 : d2;
     return KV_OK;
+}
+
+extern "C" int paged_decode_attention_noalloc(void* out, int out_dtype, const void* q,
+                                              const void* k_cache, const void* v_cache,
+                                              int kv_dtype, float k_scale, float v_scale,
+                                              int num_blocks, const int32_t* block_tables,
+                                              int max_blocks_per_seq, const int32_t* context_lens,
+                                              int num_seqs, int num_q_heads, int num_kv_heads,
+                                              int head_dim, float scale, void* stream)
+{
+    if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
+    if (num_seqs == 0) return KV_OK;
+    size_t need = 0;
+    if (int rc = paged_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              kv_dtype, &need))
+        return rc;
+    if (need > kStaticWorkspaceBytes) return KV_ERR_TOO_LARGE;
+    void* ws = nullptr;
+    if (int rc = static_workspace(&ws)) return rc;
+    return paged_decode_attention_timed(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale,
+                                        v_scale, num_blocks, block_tables, max_blocks_per_seq,
+                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                        head_dim, scale, ws, kStaticWorkspaceBytes, stream,
+                                        nullptr, nullptr, nullptr);
 }
