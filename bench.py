@@ -314,14 +314,43 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
     kv_bytes = case.logical_kv_bytes()
 
-    def step(evs=None):
+    def step():
+        # one decode step of the layer: append the new token and attend, one launch
+        pk.paged_decode_step(out, q, k_new, v_new, kc, vc, bt, cl, case.scale, ws,
+                             case.k_scale, case.v_scale, stream=stream)
+
+    def step_unfused(evs):
         pk.kv_append(k_new, v_new, kc, vc, slots, case.k_scale, case.v_scale, stream=stream)
-        if evs is None:
-            pk.paged_decode_attention(out, q, kc, vc, bt, cl, case.scale, ws,
-                                      case.k_scale, case.v_scale, stream=stream)
-        else:
-            pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
-                                            case.k_scale, case.v_scale, stream=stream)
+        pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
+                                        case.k_scale, case.v_scale, stream=stream)
+
+    def step_split_timed(evs):
+        pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
+                                        case.k_scale, case.v_scale, stream=stream)
+
+    def timed(K, body, nev):
+        """Run exactly K steps between a barrier + sync on both sides; events
+        ev[i][0..nev-1] are handed to the body of step i."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
+        for e in ev:                  # create the event handles before the timed region
+            for x in e:
+                x.record(stream)
+        t_beg = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_beg.record(stream)
+        for i in range(K):
+            body(ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return t_beg.elapsed_time(t_end) / K, ev
+
+    def unfused_body(e):
+        e[0].record(stream)
+        step_unfused(e[1:])
 
     # warm-up (W >= 3), then a short untimed soak while the clock sampler runs
     for _ in range(max(args.warmup, 3)):
@@ -335,77 +364,64 @@ def run_ours(args):
             step()
         torch.cuda.synchronize()
 
-    # timed region: exactly K steps
+    # timed region: exactly K back-to-back steps (no events between them)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for e in ev:                      # create the event handles before the timed region
-        for x in e:
-            x.record(stream)
-    t_beg = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    t_beg.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        step(ev[i][1:])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    ms_local, _ = timed(K, lambda e: step(), 0)
     clocks = sampler.stop()
-
-    ms_local = t_beg.elapsed_time(t_end) / K
-    append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-    split_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
-    combine_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(K))
     ms = reduce_max(ms_local, world, device)
     total_bytes = reduce_sum(float(kv_bytes), world, device)
     value = total_bytes / (ms * 1e-3) / 1e9
     flags, detail = pk.get_device_error()
     assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
 
+    # per-kernel durations: the same kernels with events around each launch
+    for _ in range(max(args.warmup, 3)):
+        step_split_timed([None, None, None])
+    _, sp_ev = timed(K, step_split_timed, 3)
+    split_ms = statistics.mean(sp_ev[i][0].elapsed_time(sp_ev[i][1]) for i in range(K))
+    merge_ms = statistics.mean(sp_ev[i][1].elapsed_time(sp_ev[i][2]) for i in range(K))
+
+    # the same step as separate launches (kv_append, then paged_decode_attention)
+    for _ in range(max(args.warmup, 3)):
+        step_unfused([None, None, None])
+    un_ms_local, un_ev = timed(K, unfused_body, 4)
+    unfused = {"us_per_step": reduce_max(un_ms_local, world, device) * 1e3,
+               "append_us": statistics.mean(un_ev[i][0].elapsed_time(un_ev[i][1])
+                                            for i in range(K)) * 1e3,
+               "split_us": statistics.mean(un_ev[i][1].elapsed_time(un_ev[i][2])
+                                           for i in range(K)) * 1e3,
+               "merge_us": statistics.mean(un_ev[i][2].elapsed_time(un_ev[i][3])
+                                           for i in range(K)) * 1e3}
+
     # end to end through the public API with host buffers: H2D of the step's
-    # inputs (pinned), append + attention, D2H of the output, every step
+    # inputs (pinned), the fused step, D2H of the output, every step
     e2e = None
     if not args.no_e2e:
         h_q = q.cpu().pin_memory()
         h_k = k_new.cpu().pin_memory()
         h_v = v_new.cpu().pin_memory()
-        h_slots = torch.from_numpy(slots_np).pin_memory()
         h_bt = torch.from_numpy(case.block_tables).pin_memory()
         h_cl = torch.from_numpy(case.context_lens).pin_memory()
         h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
         d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-        d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
+        d_bt, d_cl = torch.empty_like(bt), torch.empty_like(cl)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_cl))
         d2h = h_out.numel() * h_out.element_size()
 
-        def e2e_step():
+        def e2e_step(_e=None):
             d_q.copy_(h_q, non_blocking=True)
             d_k.copy_(h_k, non_blocking=True)
             d_v.copy_(h_v, non_blocking=True)
-            d_slots.copy_(h_slots, non_blocking=True)
             d_bt.copy_(h_bt, non_blocking=True)
             d_cl.copy_(h_cl, non_blocking=True)
-            pk.kv_append(d_k, d_v, kc, vc, d_slots, case.k_scale, case.v_scale, stream=stream)
-            pk.paged_decode_attention(out, d_q, kc, vc, d_bt, d_cl, case.scale, ws,
-                                      case.k_scale, case.v_scale, stream=stream)
+            pk.paged_decode_step(out, d_q, d_k, d_v, kc, vc, d_bt, d_cl, case.scale, ws,
+                                 case.k_scale, case.v_scale, stream=stream)
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(max(args.warmup, 3)):
             e2e_step()
-        torch.cuda.synchronize()
-        barrier(world)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        e2e_ms = reduce_max(e0.elapsed_time(e1) / K, world, device)
+        e2e_ms_local, _ = timed(K, e2e_step, 0)
+        e2e_ms = reduce_max(e2e_ms_local, world, device)
         e2e = {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -419,8 +435,7 @@ def run_ours(args):
                 "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
-                "split_us": split_ms * 1e3, "combine_us": combine_ms * 1e3,
-                "append_us": append_ms * 1e3}
+                "split_us": split_ms * 1e3, "merge_us": merge_ms * 1e3}
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": ms,
@@ -432,7 +447,8 @@ def run_ours(args):
             "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
             "config": dict(workload_config(cfg),
                            parallelism="replicas x%d" % world if world > 1 else "single GPU"),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks}
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
+            "unfused": unfused}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     if rank == 0:

@@ -184,11 +184,12 @@ int kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32
 
 /* --------------------------------------------------- GPU: decode attention */
 
-/* Workspace bytes paged_decode_attention needs on the current device for
- * this shape (split-KV partial outputs, their log-sum-exp terms and a small
- * per-(sequence, KV head) table).  Queries the device; KV_ERR_CUDA without
- * one.  The workspace needs no initialisation and carries nothing from one
- * call to the next; calls that overlap on the GPU need separate workspaces. */
+/* Workspace bytes paged_decode_attention / paged_decode_step need on the
+ * current device for this shape: split-KV partial outputs with their (max,
+ * sum) terms, and a small per-(sequence, KV head) table.  Queries the device;
+ * KV_ERR_CUDA without one.  The workspace needs no initialisation and carries
+ * nothing from one call to the next; calls that overlap on the GPU need
+ * separate workspaces. */
 int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int kv_dtype, size_t* bytes);
 
@@ -212,11 +213,16 @@ int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads
  * attention mask and KV cache inference", section "Padding mask and batch
  * length"; the formula of "KV Cache" (heepie), section "Self-Attention").
  * The softmax runs as an online (running max, running sum) pass over 16-token
- * blocks, split across warps and merged with the log-sum-exp rule ("KV Cache,
- * Flash Attention and inference optimization", section "Numerical trick":
- * the running (max, sum) makes the tiled result exact).  A sequence with
- * context_lens[s] == 0 gets zeros.  Deterministic: the same inputs on the
- * same device give bit-identical outputs, whatever the physical block ids. */
+ * blocks, split evenly across the warps of one persistent launch; warps that
+ * share a (sequence, KV head) leave partial results that a second, small
+ * kernel merges with the log-sum-exp rule ("KV Cache, Flash Attention and
+ * inference optimization", section "Numerical trick": the running (max, sum)
+ * makes the tiled result exact).  A sequence with context_lens[s] == 0 gets
+ * zeros.  Both kernels use programmatic dependent launch: each may start
+ * while the previous kernel on the stream drains, and waits on the device for
+ * it to finish before reading or writing any buffer.  Deterministic: the same
+ * inputs on the same device give bit-identical outputs, whatever the physical
+ * block ids.  `out` must be 16-byte aligned. */
 int paged_decode_attention(void* out, int out_dtype, const void* q, const void* k_cache,
                            const void* v_cache, int kv_dtype, float k_scale, float v_scale,
                            int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
@@ -235,8 +241,32 @@ int paged_decode_attention_timed(void* out, int out_dtype, const void* q, const 
                                  int max_blocks_per_seq, const int32_t* context_lens,
                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  float scale, void* workspace, size_t workspace_bytes,
-                                 void* stream, void* ev_split_begin, void* ev_split_end,
-                                 void* ev_combine_end);
+                                 void* stream, void* ev_begin, void* ev_split_end, void* ev_end);
+
+/* A whole decode step of one layer: append each sequence's new
+ * token, then attend (the order of "Transformer attention mask and KV cache
+ * inference", section "Prefill and decode phases").  Same arguments as
+ * paged_decode_attention, plus
+ *   k_new, v_new:  [num_seqs][num_kv_heads][head_dim] bfloat16 (device), the
+ *                  new token's K and V of every sequence;
+ *   k_cache, v_cache are written: the new token of sequence s is stored at
+ *                  position context_lens[s]-1, i.e. slot
+ *                  block_tables[s][(L-1)/16]*16 + (L-1)%16 (the append
+ *                  contract of the same page, section "Position ID and append
+ *                  contract"), with the same bits as kv_append (bf16 copy or
+ *                  E4M3(x/scale)), and is attended to in the same launch.
+ * context_lens are the lengths after the append (as for
+ * paged_decode_attention).  The block receiving a new token must be private
+ * to its sequence (kv_step's copy-on-write guarantees it); sequences with
+ * context_lens[s] == 0 append nothing.  Equivalent to kv_append with
+ * slot_mapping = kv_slot_mapping(block_tables, context_lens-1) followed by
+ * paged_decode_attention. */
+int paged_decode_step(void* out, int out_dtype, const void* q, const void* k_new,
+                      const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                      float k_scale, float v_scale, int num_blocks, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free variant of paged_decode_attention for callers that cannot
  * allocate device memory: code running inside a host framework that owns the

@@ -82,6 +82,8 @@ _SIGS = {
                                     _i, _f, _p, ctypes.c_size_t, _p]),
     "paged_decode_attention_timed": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
                                           _i, _i, _i, _f, _p, ctypes.c_size_t, _p, _p, _p, _p]),
+    "paged_decode_step": (_i, [_p, _i, _p, _p, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i,
+                               _i, _i, _f, _p, ctypes.c_size_t, _p]),
     "paged_decode_attention_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
                                             _i, _i, _i, _f, _p]),
     "kv_get_device_error": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_i64)]),
@@ -277,20 +279,37 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
 def paged_decode_attention_timed(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                                  workspace, events, k_scale=1.0, v_scale=1.0, stream=None):
     """paged_decode_attention that also records three torch.cuda.Event objects
-    (already recorded once, so that their handles exist) around the split and
-    merge launches: events = (before split, after split, after merge)."""
+    (already recorded once, so that their handles exist, or None) before the
+    split kernel, after it and after the merge kernel: events = (begin,
+    split_end, end)."""
     import torch
     B, Hq, D = q.shape
     NB, Hkv, _, _ = k_cache.shape
     out_dtype = F32 if out.dtype == torch.float32 else BF16
-    ev = [ctypes.c_void_p(e._as_parameter_.value if hasattr(e._as_parameter_, "value")
-                          else e._as_parameter_) for e in events]
+    ev = [ctypes.c_void_p(e._as_parameter_.value) if e is not None else None for e in events]
     _check(_lib.paged_decode_attention_timed(
         _dptr(out), out_dtype, _dptr(q), _dptr(k_cache), _dptr(v_cache), _cache_dtype(k_cache),
         float(k_scale), float(v_scale), NB, _dptr(block_tables), block_tables.shape[1],
         _dptr(context_lens), B, Hq, Hkv, D, float(scale), _dptr(workspace),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream), ev[0], ev[1], ev[2]),
         "paged_decode_attention_timed")
+
+
+def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                      workspace, k_scale=1.0, v_scale=1.0, stream=None):
+    """One decode step in one launch: append k_new/v_new ([B, Hkv, D] bfloat16)
+    at position context_lens-1 of each sequence, then attend (see
+    paged_decode_attention for the other arguments)."""
+    import torch
+    B, Hq, D = q.shape
+    NB, Hkv, _, _ = k_cache.shape
+    out_dtype = F32 if out.dtype == torch.float32 else BF16
+    _check(_lib.paged_decode_step(
+        _dptr(out), out_dtype, _dptr(q), _dptr(k_new), _dptr(v_new), _dptr(k_cache),
+        _dptr(v_cache), _cache_dtype(k_cache), float(k_scale), float(v_scale), NB,
+        _dptr(block_tables), block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D,
+        float(scale), _dptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream)), "paged_decode_step")
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

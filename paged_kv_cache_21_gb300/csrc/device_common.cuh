@@ -3,6 +3,7 @@
 
 #include <cstdint>
 
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 namespace pkv {
@@ -144,6 +145,18 @@ __device__ __forceinline__ void lds64(uint32_t (&r)[2], uint32_t addr)
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint2 v)
+{
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1)
@@ -185,5 +198,26 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Eight bfloat16 (one 16-byte chunk) -> eight E4M3 codes of x / s: the
+// quotient is an IEEE binary32 division, then round to nearest even with
+// saturation to +-448 (NaN stays NaN).  Byte i holds element i.
+__device__ __forceinline__ uint2 quantize8_e4m3(uint4 x, float s)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t packed[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float2 a, b;
+        a.x = __fdiv_rn(bf16_lo(w[2 * j]), s);
+        a.y = __fdiv_rn(bf16_hi(w[2 * j]), s);
+        b.x = __fdiv_rn(bf16_lo(w[2 * j + 1]), s);
+        b.y = __fdiv_rn(bf16_hi(w[2 * j + 1]), s);
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+        packed[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    return make_uint2(packed[0], packed[1]);
+}
 
 }  // namespace pkv

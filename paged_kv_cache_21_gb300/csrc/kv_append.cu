@@ -59,22 +59,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
         if (!FP8) {
             *reinterpret_cast<uint4*>(cache + dst * 2) = x;
         } else {
-            const float s = is_v ? v_scale : k_scale;
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-            uint32_t packed[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                __nv_fp8x2_storage_t lo, hi;
-                float2 a, b;
-                a.x = __fdiv_rn(bf16_lo(w[2 * j]), s);
-                a.y = __fdiv_rn(bf16_hi(w[2 * j]), s);
-                b.x = __fdiv_rn(bf16_lo(w[2 * j + 1]), s);
-                b.y = __fdiv_rn(bf16_hi(w[2 * j + 1]), s);
-                lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
-                hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
-                packed[j] = (uint32_t)lo | ((uint32_t)hi << 16);
-            }
-            *reinterpret_cast<uint2*>(cache + dst) = make_uint2(packed[0], packed[1]);
+            *reinterpret_cast<uint2*>(cache + dst) = quantize8_e4m3(x, is_v ? v_scale : k_scale);
         }
     }
 }

@@ -27,8 +27,18 @@
 //    fragment of the score MMA is exactly the B fragment of the PV MMA, so
 //    scores never leave registers.
 //  * Warps whose range covers a whole (sequence, KV head) write the output
-//    directly; the others write an unnormalised partial output with its
-//    (max, sum) and a second kernel merges them by the log-sum-exp rule.
+//    directly; the others store an unnormalised partial output with its
+//    (max, sum) -- plain stores, no atomics or fences, so the split kernel
+//    ends as soon as its last tile is consumed -- and a small merge kernel
+//    combines them by the log-sum-exp rule in warp order (deterministic).
+//    Both kernels use programmatic dependent launch: each is launched while
+//    the previous kernel on the stream drains and waits on the device
+//    (griddepcontrol.wait) before touching memory, which hides the launch
+//    latency between them.
+//  * Optionally (paged_decode_step) the append of the step's new token is
+//    fused in: the warp that owns a pair's last block writes the new K/V to
+//    the cache and patches its own copy of that tile in shared memory before
+//    using it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -82,18 +92,23 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c)
     return (uint32_t)(box * G::BOXB) + (a ^ (((a >> 7) & G::SWZ) << 4));
 }
 
-struct SplitParams {
+struct DecodeParams {
     const uint16_t* q;       // bf16 [B][Hq][D]
     void* out;               // [B][Hq][D] bf16 or f32
     const int32_t* bt;       // [B][max_blocks]
     const int32_t* ctx;      // [B]
     float* part_o;           // [slots][G][D]
     float2* part_ml;         // [slots][G]  (max in log2 units, sum)
-    int2* pair_meta;         // [B*Hkv]     (first warp, number of partials)
+    int2* pair_meta;         // [B*Hkv]  (first warp, number of partials)
+    const uint16_t* k_new;   // bf16 [B][Hkv][D], or null: no append
+    const uint16_t* v_new;
+    uint8_t* k_cache;        // caches, written only by the fused append
+    uint8_t* v_cache;
     int B, Hq, Hkv, G, max_blocks, num_blocks;
     int warps_total;
     float sl2;               // scale * log2(e) (* k_scale)
     float v_scale;
+    float k_qscale, v_qscale;    // quantisation scales of the fused append (E4M3)
     int out_f32;
 };
 
@@ -136,7 +151,7 @@ struct Win {
 // Fill the window for flat positions pos0 + lane (relative to the warp's
 // range start), walking forward from cursor (s, h, blk) where blk may equal
 // the pair's block count (then the walk moves on to the next pair).
-__device__ __forceinline__ void fill_window(Win& e, const SplitParams& p, int s, int h, int blk,
+__device__ __forceinline__ void fill_window(Win& e, const DecodeParams& p, int s, int h, int blk,
                                             int nb, int L, int pos0, int cnt, int lane)
 {
     e.id = -1; e.s = 0; e.h = 0; e.blk = 0; e.L = 0;
@@ -324,7 +339,7 @@ __device__ __forceinline__ void block_fp8(uint32_t kbase, uint32_t vbase, int nv
 
 // Query fragments of head (h*G + g) of sequence s (rows g >= G are zero).
 template <int D, bool FP8>
-__device__ __forceinline__ void load_q(const SplitParams& p, int s, int h, int lane,
+__device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, int lane,
                                        uint32_t (&qa0)[D / 16], uint32_t (&qa2)[D / 16])
 {
     const int g = lane >> 2, t = lane & 3;
@@ -345,11 +360,38 @@ __device__ __forceinline__ void load_q(const SplitParams& p, int s, int h, int l
     }
 }
 
-// End of a segment: write the final output (whole pair) or a partial.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class P>
+__device__ __forceinline__ void store4(const P& p, size_t idx, float a, float b, float c, float d)
+{
+    if (p.out_f32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + idx) = make_float4(a, b, c, d);
+    } else {
+        uint2 v;
+        v.x = pack_bf16x2(a, b);
+        v.y = pack_bf16x2(c, d);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + idx) = v;
+    }
+}
+
+// End of a segment (a run of blocks of one pair inside this warp's range):
+// write the final output if the warp saw the whole pair, otherwise store a
+// partial for the merge kernel.  The warp holding the pair's block 0 also
+// records which warps hold the rest.  Only plain stores: a pair switch in
+// mid-range does not stall the warp's pipeline.
 template <int D, bool FP8>
-__device__ __forceinline__ void finalize(const SplitParams& p, int w, int q, int b0, int s, int h,
-                                         int first_blk, int last_blk, int L, int i0, float m,
-                                         float l, const float (&o)[D / 16][4], int lane)
+__device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, int s, int h,
+                                         int first_blk, int last_blk, int L, int flat_first,
+                                         float m, float l, const float (&o)[D / 16][4], int lane)
 {
     const int g = lane >> 2, t = lane & 3;
     float lt = l + __shfl_xor_sync(kFull, l, 1);
@@ -358,9 +400,8 @@ __device__ __forceinline__ void finalize(const SplitParams& p, int w, int q, int
     const float ma = __shfl_sync(kFull, m, 8 * t), mb = __shfl_sync(kFull, m, 8 * t + 4);
     const int nb = (L + kBlock - 1) / kBlock;
     const int pair = s * p.Hkv + h;
-    const bool whole = first_blk == 0 && last_blk == nb - 1;
     const int ha = 2 * t, hb = 2 * t + 1;
-    if (whole) {
+    if (first_blk == 0 && last_blk == nb - 1) {
         const float ia = la > 0.f ? p.v_scale / la : 0.f;
         const float ib = lb > 0.f ? p.v_scale / lb : 0.f;
         const size_t row = (size_t)s * p.Hq + (size_t)h * p.G;
@@ -401,16 +442,48 @@ __device__ __forceinline__ void finalize(const SplitParams& p, int w, int q, int
         }
     }
     if (first_blk == 0 && lane == 0) {
-        // this warp holds block 0 of the pair: record who holds the rest
-        const int w_last = (b0 + i0 + nb - 1) / q;
+        // block 0 of the pair is here: record the warps whose ranges meet its
+        // blocks [flat_first, flat_first + nb)
+        const int w_last = (flat_first + nb - 1) / q;
         p.pair_meta[pair] = make_int2(w, w_last - w + 1);
     }
+}
+
+// The fused append of the step's new token of pair (s, h): position L-1,
+// i.e. row (L-1) % 16 of the pair's last block `id`.  Writes the cache in
+// global memory and the same bytes into this warp's copy of the tile in
+// shared memory (which the bulk copy may have filled before the write).
+template <int D, bool FP8>
+__device__ __forceinline__ void append_patch(const DecodeParams& p, int s, int h, int id, int L,
+                                             uint32_t kst, uint32_t vst, int lane)
+{
+    using G = Geom<D, FP8>;
+    constexpr int CH = D / 8;              // groups of 8 elements per row
+    if (lane < 2 * CH) {
+        const bool isv = lane >= CH;
+        const int c = isv ? lane - CH : lane;
+        const int r = (L - 1) & (kBlock - 1);
+        const size_t src = ((size_t)s * p.Hkv + h) * D + 8 * c;
+        const size_t dst = (((size_t)id * p.Hkv + h) * kBlock + r) * D + 8 * c;
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src));
+        uint8_t* cache = isv ? p.v_cache : p.k_cache;
+        const uint32_t sb = isv ? vst : kst;
+        if (!FP8) {
+            *reinterpret_cast<uint4*>(cache + dst * 2) = x;
+            sts128(sb + tile_off<G>(r, c), x);
+        } else {
+            const uint2 y = quantize8_e4m3(x, isv ? p.v_qscale : p.k_qscale);
+            *reinterpret_cast<uint2*>(cache + dst) = y;
+            sts64(sb + tile_off<G>(r, c >> 1) + 8 * (c & 1), y);
+        }
+    }
+    __syncwarp();
 }
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const SplitParams p)
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
 {
     using G = Geom<D, FP8>;
     constexpr int ST = G::STAGES;
@@ -430,6 +503,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
+    // let the next kernel on the stream launch now, then wait until the
+    // previous one has finished and its writes are visible
+    pdl_launch_dependents();
+    pdl_wait();
 
     // ---- 1. total work and this warp's range --------------------------------
     constexpr int U = 8;           // first 256 sequences stay in registers
@@ -529,7 +606,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int L = __shfl_sync(kFull, cur.L, src);
         if (lane == 0) {
             const bool valid = id >= 0 && id < p.num_blocks;
-            meta[st] = make_int4(s, valid ? h : -1 - h, blk, L);
+            const int pair = s * p.Hkv + h;
+            meta[st] = make_int4(valid ? pair : -1 - pair, blk, L, id);
             const uint32_t bar = bar0 + st * 8;
             const uint32_t dst = stage0 + (uint32_t)(st * G::STAGE);
             if (valid) {
@@ -578,12 +656,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             return;
         }
         const int4 mt = meta[st];
-        const bool valid = mt.y >= 0;
-        const int s = mt.x, h = valid ? mt.y : -1 - mt.y, blk = mt.z, L = mt.w;
+        const bool valid = mt.x >= 0;
+        const int pair = valid ? mt.x : -1 - mt.x;
+        const int s = pair / p.Hkv, h = pair - s * p.Hkv, blk = mt.y, L = mt.z;
         if (s != seg_s || h != seg_h) {
             if (seg_s >= 0)
-                finalize<D, FP8>(p, w, q, b0, seg_s, seg_h, seg_first, seg_last, seg_L, seg_i0, m,
-                                 l, o, lane);
+                finalize<D, FP8>(p, w, q, seg_s, seg_h, seg_first, seg_last, seg_L, b0 + seg_i0,
+                                 m, l, o, lane);
             seg_s = s; seg_h = h; seg_first = blk; seg_L = L; seg_i0 = i;
             load_q<D, FP8>(p, s, h, lane, qa0, qa2);
             m = -INFINITY;
@@ -595,6 +674,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (valid) {
             const int nvalid = min(kBlock, L - blk * kBlock);
             const uint32_t kb = stage0 + (uint32_t)(st * G::STAGE);
+            if (p.k_new != nullptr && nvalid == L - blk * kBlock)     // the pair's last block
+                append_patch<D, FP8>(p, s, h, mt.w, L, kb, kb + G::TILE, lane);
             if (FP8) block_fp8<D>(kb, kb + G::TILE, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
             else block_bf16<D>(kb, kb + G::TILE, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
         }
@@ -603,37 +684,47 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (++st == ST) { st = 0; phase ^= 1u; }
     }
     if (seg_s >= 0)
-        finalize<D, FP8>(p, w, q, b0, seg_s, seg_h, seg_first, seg_last, seg_L, seg_i0, m, l, o,
+        finalize<D, FP8>(p, w, q, seg_s, seg_h, seg_first, seg_last, seg_L, b0 + seg_i0, m, l, o,
                          lane);
 }
 
-// ------------------------------------------------------------------ combine
+// -------------------------------------------------------------------- merge
 
-struct CombineParams {
+struct MergeParams {
     void* out;
     const int32_t* ctx;
     const float* part_o;
     const float2* part_ml;
     const int2* pair_meta;
-    int B, Hq, Hkv, G, D, max_blocks;
+    int B, Hq, Hkv, G, max_blocks;
     int nslots;              // partial slots in the workspace
     int out_f32;
 };
 
-// One CTA per (sequence, KV head): merge the partial outputs of the warps
-// that shared it, out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
-__global__ void __launch_bounds__(128) paged_decode_combine_kernel(const CombineParams p)
+// One CTA per (sequence, KV head): merge the partials the split kernel left
+// for it (pairs seen whole by one warp were written there already), or write
+// zeros for an empty context.  Thread t owns output float4 column t of the
+// pair's G x D block; the (max, sum) terms of up to 64 partials at a time go
+// through shared memory, and a thread's partial loads are independent of one
+// another, so the merge costs a few L2 round trips.
+constexpr int kMergeThreads = 256;   // >= 8 heads x 128 / 4 columns
+constexpr int kMergeChunk = 64;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads, 1) paged_decode_merge_kernel(const MergeParams p)
 {
+    __shared__ float2 sml[kMergeChunk * 8];
+    pdl_launch_dependents();
+    pdl_wait();
     const int pair = blockIdx.x;
     const int s = pair / p.Hkv, h = pair - s * p.Hkv;
+    const int t = threadIdx.x;
+    const int cols = p.G * (D / 4);
+    const size_t row = (size_t)s * p.Hq + (size_t)h * p.G;
     int L;
     seq_blocks(p.ctx, s, p.max_blocks, L);
-    const size_t row = (size_t)s * p.Hq + (size_t)h * p.G;
     if (L <= 0) {
-        for (int idx = threadIdx.x; idx < p.G * p.D; idx += blockDim.x) {
-            if (p.out_f32) reinterpret_cast<float*>(p.out)[row * p.D + idx] = 0.f;
-            else reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.D + idx] = __float2bfloat16_rn(0.f);
-        }
+        if (t < cols) store4(p, row * D + 4 * t, 0.f, 0.f, 0.f, 0.f);
         return;
     }
     const int2 mt = p.pair_meta[pair];
@@ -643,20 +734,45 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const Combine
     // would leave the workspace (only an aborted split launch leaves it stale)
     if (mt.x < 0 || (long long)pair + mt.x + n > (long long)p.nslots) return;
     const size_t slot0 = (size_t)pair + mt.x;
-    for (int idx = threadIdx.x; idx < p.G * p.D; idx += blockDim.x) {
-        const int gq = idx / p.D;
-        float M = -INFINITY;
-        for (int k = 0; k < n; ++k) M = fmaxf(M, p.part_ml[(slot0 + k) * p.G + gq].x);
-        float num = 0.f, den = 0.f;
-        for (int k = 0; k < n; ++k) {
-            const float2 ml = p.part_ml[(slot0 + k) * p.G + gq];
-            const float f = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
-            num += f * p.part_o[(slot0 + k) * p.G * p.D + idx];
-            den += f * ml.y;
+    const int g = t / (D / 4), d4 = t % (D / 4);
+    const bool live = t < cols;
+    float M = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < n; k0 += kMergeChunk) {
+        const int nk = min(kMergeChunk, n - k0);
+        __syncthreads();
+        for (int i = t; i < nk * p.G; i += kMergeThreads) {
+            const int kk = i / p.G, gg = i - kk * p.G;
+            float2 v = __ldcg(&p.part_ml[(slot0 + k0 + kk) * p.G + gg]);
+            if (!(v.y > 0.f)) v = make_float2(-INFINITY, 0.f);     // empty partial
+            sml[kk * 8 + gg] = v;
         }
-        const float v = den > 0.f ? num / den : 0.f;
-        if (p.out_f32) reinterpret_cast<float*>(p.out)[row * p.D + idx] = v;
-        else reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.D + idx] = __float2bfloat16_rn(v);
+        __syncthreads();
+        if (!live) continue;
+        float cm = -INFINITY;
+        for (int k = 0; k < nk; ++k) cm = fmaxf(cm, sml[k * 8 + g].x);
+        const float Mn = fmaxf(M, cm);
+        const float r = Mn == -INFINITY ? 0.f : exp2f(M - Mn);
+        den *= r;
+        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+        M = Mn;
+        const float4* po = reinterpret_cast<const float4*>(p.part_o + (slot0 + k0) * p.G * D) +
+                           (size_t)g * (D / 4) + d4;
+#pragma unroll 8
+        for (int k = 0; k < nk; ++k) {
+            const float4 o = __ldcg(po + (size_t)k * p.G * (D / 4));
+            const float2 v = sml[k * 8 + g];
+            const float f = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+            den += f * v.y;
+            acc.x += f * o.x;
+            acc.y += f * o.y;
+            acc.z += f * o.z;
+            acc.w += f * o.w;
+        }
+    }
+    if (live) {
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        store4(p, (row + g) * D + 4 * d4, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
 }
 
@@ -795,11 +911,146 @@ int check_shape(int num_seqs, int Hq, int Hkv, int D, int kv_dtype)
     return KV_OK;
 }
 
-template <int D, bool FP8>
-void launch_split(int grid, const CUtensorMap& mk, const CUtensorMap& mv, const SplitParams& sp,
-                  cudaStream_t st)
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream drains; it waits on the device
+// (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t st, Args... args)
 {
-    paged_decode_split_kernel<D, FP8><<<grid, kWarps * 32, Geom<D, FP8>::SMEM, st>>>(mk, mv, sp);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+struct AppendArgs {
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+};
+
+// Validate, build the tensor maps and launch the decode kernel (one launch).
+int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
+                  const void* v_cache, int kv_dtype, float k_scale, float v_scale, int num_blocks,
+                  const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                  int head_dim, float scale, void* workspace, size_t workspace_bytes,
+                  void* stream, const AppendArgs* app, void* ev_begin, void* ev_split,
+                  void* ev_end)
+{
+    if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
+    if (out_dtype != KV_DTYPE_BF16 && out_dtype != KV_DTYPE_F32) return KV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+        return KV_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || max_blocks_per_seq <= 0) return KV_ERR_INVALID_ARG;
+    if ((((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)workspace |
+          (uintptr_t)out) & 15) != 0)
+        return KV_ERR_INVALID_ARG;
+    if (app && (!app->k_new || !app->v_new ||
+                (((uintptr_t)app->k_new | (uintptr_t)app->v_new) & 15) != 0))
+        return KV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+    const bool fp8 = kv_dtype == KV_DTYPE_FP8_E4M3;
+    if (fp8 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
+        return KV_ERR_INVALID_ARG;
+    // flat work indices and tensor-map rows must fit in int32
+    if ((long long)num_seqs * max_blocks_per_seq * num_kv_heads >= INT_MAX ||
+        (long long)num_blocks * num_kv_heads >= INT_MAX ||
+        (long long)max_blocks_per_seq * kBlock >= INT_MAX)
+        return KV_ERR_UNSUPPORTED;
+
+    int sms = 0, cps = 0;
+    if (int rc = device_info(head_dim, fp8, sms, cps)) return rc;
+    const int grid = sms * cps;
+    const int warps_total = grid * kWarps;
+    const WsLayout ws = ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, warps_total);
+    if (workspace_bytes < ws.total) return KV_ERR_INVALID_ARG;
+
+    CUtensorMap mk, mv;
+    if (int rc = make_cache_map(&mk, k_cache, head_dim, fp8, num_blocks, num_kv_heads)) return rc;
+    if (int rc = make_cache_map(&mv, v_cache, head_dim, fp8, num_blocks, num_kv_heads)) return rc;
+
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    DecodeParams dp;
+    dp.q = static_cast<const uint16_t*>(q);
+    dp.out = out;
+    dp.bt = block_tables;
+    dp.ctx = context_lens;
+    dp.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
+    dp.part_ml = reinterpret_cast<float2*>(wsb + ws.part_ml);
+    dp.pair_meta = reinterpret_cast<int2*>(wsb + ws.meta);
+    dp.k_new = app ? static_cast<const uint16_t*>(app->k_new) : nullptr;
+    dp.v_new = app ? static_cast<const uint16_t*>(app->v_new) : nullptr;
+    dp.k_cache = app ? static_cast<uint8_t*>(app->k_cache) : nullptr;
+    dp.v_cache = app ? static_cast<uint8_t*>(app->v_cache) : nullptr;
+    dp.B = num_seqs;
+    dp.Hq = num_q_heads;
+    dp.Hkv = num_kv_heads;
+    dp.G = num_q_heads / num_kv_heads;
+    dp.max_blocks = max_blocks_per_seq;
+    dp.num_blocks = num_blocks;
+    dp.warps_total = warps_total;
+    dp.sl2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
+    dp.v_scale = fp8 ? v_scale : 1.f;
+    dp.k_qscale = k_scale;
+    dp.v_qscale = v_scale;
+    dp.out_f32 = out_dtype == KV_DTYPE_F32;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (ev_begin && cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), st) != cudaSuccess)
+        return KV_ERR_CUDA;
+    const int threads = kWarps * 32;
+    cudaError_t err;
+    if (head_dim == 128) {
+        if (fp8)
+            err = launch_pdl(paged_decode_split_kernel<128, true>, grid, threads,
+                             Geom<128, true>::SMEM, st, mk, mv, dp);
+        else
+            err = launch_pdl(paged_decode_split_kernel<128, false>, grid, threads,
+                             Geom<128, false>::SMEM, st, mk, mv, dp);
+    } else {
+        if (fp8)
+            err = launch_pdl(paged_decode_split_kernel<64, true>, grid, threads,
+                             Geom<64, true>::SMEM, st, mk, mv, dp);
+        else
+            err = launch_pdl(paged_decode_split_kernel<64, false>, grid, threads,
+                             Geom<64, false>::SMEM, st, mk, mv, dp);
+    }
+    if (err != cudaSuccess) return KV_ERR_CUDA;
+    if (ev_split && cudaEventRecord(static_cast<cudaEvent_t>(ev_split), st) != cudaSuccess)
+        return KV_ERR_CUDA;
+
+    MergeParams mp;
+    mp.out = out;
+    mp.ctx = context_lens;
+    mp.part_o = dp.part_o;
+    mp.part_ml = dp.part_ml;
+    mp.pair_meta = dp.pair_meta;
+    mp.B = num_seqs;
+    mp.Hq = num_q_heads;
+    mp.Hkv = num_kv_heads;
+    mp.G = dp.G;
+    mp.max_blocks = max_blocks_per_seq;
+    mp.nslots = num_seqs * num_kv_heads + warps_total;
+    mp.out_f32 = dp.out_f32;
+    const unsigned mgrid = (unsigned)(num_seqs * num_kv_heads);
+    err = head_dim == 128
+              ? launch_pdl(paged_decode_merge_kernel<128>, mgrid, kMergeThreads, 0, st, mp)
+              : launch_pdl(paged_decode_merge_kernel<64>, mgrid, kMergeThreads, 0, st, mp);
+    if (err != cudaSuccess) return KV_ERR_CUDA;
+    if (ev_end && cudaEventRecord(static_cast<cudaEvent_t>(ev_end), st) != cudaSuccess)
+        return KV_ERR_CUDA;
+    return KV_OK;
 }
 
 }  // namespace
@@ -877,91 +1128,12 @@ extern "C" int paged_decode_attention_timed(
     int kv_dtype, float k_scale, float v_scale, int num_blocks, const int32_t* block_tables,
     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, float scale, void* workspace, size_t workspace_bytes,
-    void* stream, void* ev_split_begin, void* ev_split_end, void* ev_combine_end)
+    void* stream, void* ev_begin, void* ev_split_end, void* ev_end)
 {
-    if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
-    if (out_dtype != KV_DTYPE_BF16 && out_dtype != KV_DTYPE_F32) return KV_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return KV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
-        return KV_ERR_INVALID_ARG;
-    if (num_blocks <= 0 || max_blocks_per_seq <= 0) return KV_ERR_INVALID_ARG;
-    if ((((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)workspace) & 15) != 0)
-        return KV_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
-    const bool fp8 = kv_dtype == KV_DTYPE_FP8_E4M3;
-    if (fp8 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
-        return KV_ERR_INVALID_ARG;
-    // flat work indices and tensor-map rows must fit in int32
-    if ((long long)num_seqs * max_blocks_per_seq * num_kv_heads >= INT_MAX ||
-        (long long)num_blocks * num_kv_heads >= INT_MAX ||
-        (long long)max_blocks_per_seq * kBlock >= INT_MAX)
-        return KV_ERR_UNSUPPORTED;
-
-    int sms = 0, cps = 0;
-    if (int rc = device_info(head_dim, fp8, sms, cps)) return rc;
-    const int grid = sms * cps;
-    const int warps_total = grid * kWarps;
-    const WsLayout ws = ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, warps_total);
-    if (workspace_bytes < ws.total) return KV_ERR_INVALID_ARG;
-
-    CUtensorMap mk, mv;
-    if (int rc = make_cache_map(&mk, k_cache, head_dim, fp8, num_blocks, num_kv_heads)) return rc;
-    if (int rc = make_cache_map(&mv, v_cache, head_dim, fp8, num_blocks, num_kv_heads)) return rc;
-
-    uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    SplitParams sp;
-    sp.q = static_cast<const uint16_t*>(q);
-    sp.out = out;
-    sp.bt = block_tables;
-    sp.ctx = context_lens;
-    sp.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
-    sp.part_ml = reinterpret_cast<float2*>(wsb + ws.part_ml);
-    sp.pair_meta = reinterpret_cast<int2*>(wsb + ws.meta);
-    sp.B = num_seqs;
-    sp.Hq = num_q_heads;
-    sp.Hkv = num_kv_heads;
-    sp.G = num_q_heads / num_kv_heads;
-    sp.max_blocks = max_blocks_per_seq;
-    sp.num_blocks = num_blocks;
-    sp.warps_total = warps_total;
-    sp.sl2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
-    sp.v_scale = fp8 ? v_scale : 1.f;
-    sp.out_f32 = out_dtype == KV_DTYPE_F32;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (ev_split_begin && cudaEventRecord(static_cast<cudaEvent_t>(ev_split_begin), st) != cudaSuccess)
-        return KV_ERR_CUDA;
-    if (head_dim == 128) {
-        if (fp8) launch_split<128, true>(grid, mk, mv, sp, st);
-        else launch_split<128, false>(grid, mk, mv, sp, st);
-    } else {
-        if (fp8) launch_split<64, true>(grid, mk, mv, sp, st);
-        else launch_split<64, false>(grid, mk, mv, sp, st);
-    }
-    if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
-    if (ev_split_end && cudaEventRecord(static_cast<cudaEvent_t>(ev_split_end), st) != cudaSuccess)
-        return KV_ERR_CUDA;
-
-    CombineParams cp;
-    cp.out = out;
-    cp.ctx = context_lens;
-    cp.part_o = sp.part_o;
-    cp.part_ml = sp.part_ml;
-    cp.pair_meta = sp.pair_meta;
-    cp.B = num_seqs;
-    cp.Hq = num_q_heads;
-    cp.Hkv = num_kv_heads;
-    cp.G = sp.G;
-    cp.D = head_dim;
-    cp.max_blocks = max_blocks_per_seq;
-    cp.nslots = num_seqs * num_kv_heads + warps_total;
-    cp.out_f32 = sp.out_f32;
-    paged_decode_combine_kernel<<<num_seqs * num_kv_heads, 128, 0, st>>>(cp);
-    if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
-    if (ev_combine_end &&
-        cudaEventRecord(static_cast<cudaEvent_t>(ev_combine_end), st) != cudaSuccess)
-        return KV_ERR_CUDA;
-    return KV_OK;
+    return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                         num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                         stream, nullptr, ev_begin, ev_split_end, ev_end);
 }
 
 extern "C" int paged_decode_attention(void* out, int out_dtype, const void* q, const void* k_cache,
@@ -972,11 +1144,25 @@ extern "C" int paged_decode_attention(void* out, int out_dtype, const void* q, c
                                       int head_dim, float scale, void* workspace,
                                       size_t workspace_bytes, void* stream)
 {
-    return paged_decode_attention_timed(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale,
-                                        v_scale, num_blocks, block_tables, max_blocks_per_seq,
-                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
-                                        head_dim, scale, workspace, workspace_bytes, stream,
-                                        nullptr, nullptr, nullptr);
+    return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                         num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                         stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+extern "C" int paged_decode_step(void* out, int out_dtype, const void* q, const void* k_new,
+                                 const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                                 float k_scale, float v_scale, int num_blocks,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, float scale, void* workspace,
+                                 size_t workspace_bytes, void* stream)
+{
+    const AppendArgs app = {k_new, v_new, k_cache, v_cache};
+    return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                         num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                         stream, &app, nullptr, nullptr, nullptr);
 }
 
 extern "C" int kv_get_device_error(int* flags, int64_t* detail)
@@ -1007,9 +1193,8 @@ extern "C" int paged_decode_attention_noalloc(void* out, int out_dtype, const vo
     if (need > kStaticWorkspaceBytes) return KV_ERR_TOO_LARGE;
     void* ws = nullptr;
     if (int rc = static_workspace(&ws)) return rc;
-    return paged_decode_attention_timed(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale,
-                                        v_scale, num_blocks, block_tables, max_blocks_per_seq,
-                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
-                                        head_dim, scale, ws, kStaticWorkspaceBytes, stream,
-                                        nullptr, nullptr, nullptr);
+    return paged_decode_attention(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                                  num_blocks, block_tables, max_blocks_per_seq, context_lens,
+                                  num_seqs, num_q_heads, num_kv_heads, head_dim, scale, ws,
+                                  kStaticWorkspaceBytes, stream);
 }

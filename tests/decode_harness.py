@@ -29,8 +29,11 @@ def half_ulp_bf16(x):
     return np.where(ax > 0, np.exp2(e - 8), np.exp2(-134))
 
 
-def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None, stream=None):
-    """Returns (out, k_cache, v_cache) on the device."""
+def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None, stream=None,
+             fused=False, workspace=None):
+    """Returns (out, k_cache, v_cache) on the device.  fused=False: kv_append
+    then paged_decode_attention (two launches); fused=True: paged_decode_step
+    (append and attention in one launch)."""
     import paged_kv_cache_21_gb300 as pk
     NB, Hkv, D = case.num_blocks, case.Hkv, case.D
     cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
@@ -43,16 +46,22 @@ def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None,
         pool_k, pool_v = pool_overrides(pool_k, pool_v)
     pk.kv_append(pool_k, pool_v, kc, vc, all_slots, case.k_scale, case.v_scale, stream=stream)
     del pool_k, pool_v
-    slots_new = pk.slot_mapping(case.block_tables, case.context_lens.astype(np.int64) - 1)
-    pk.kv_append(case.k_new.to(device), case.v_new.to(device), kc, vc,
-                 torch.from_numpy(slots_new).to(device), case.k_scale, case.v_scale,
-                 stream=stream)
     out = torch.empty((case.B, case.Hq, D), dtype=out_dtype, device=device)
-    ws = pk.alloc_workspace(case.B, case.Hq, Hkv, D, case.kv_dtype, device=device)
+    ws = workspace if workspace is not None else pk.alloc_workspace(
+        case.B, case.Hq, Hkv, D, case.kv_dtype, device=device)
     bt = torch.from_numpy(case.block_tables).to(device)
     cl = torch.from_numpy(case.context_lens).to(device)
-    pk.paged_decode_attention(out, case.q.to(device), kc, vc, bt, cl, case.scale, ws,
-                              case.k_scale, case.v_scale, stream=stream)
+    if fused:
+        pk.paged_decode_step(out, case.q.to(device), case.k_new.to(device),
+                             case.v_new.to(device), kc, vc, bt, cl, case.scale, ws,
+                             case.k_scale, case.v_scale, stream=stream)
+    else:
+        slots_new = pk.slot_mapping(case.block_tables, case.context_lens.astype(np.int64) - 1)
+        pk.kv_append(case.k_new.to(device), case.v_new.to(device), kc, vc,
+                     torch.from_numpy(slots_new).to(device), case.k_scale, case.v_scale,
+                     stream=stream)
+        pk.paged_decode_attention(out, case.q.to(device), kc, vc, bt, cl, case.scale, ws,
+                                  case.k_scale, case.v_scale, stream=stream)
     torch.cuda.synchronize()
     return out, kc, vc
 

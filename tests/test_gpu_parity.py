@@ -36,8 +36,8 @@ def cache_bits(t):
     return t.numpy()
 
 
-def check_case(case, out_dtype=torch.bfloat16, pair_select=None, what=""):
-    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype)
+def check_case(case, out_dtype=torch.bfloat16, pair_select=None, what="", fused=False):
+    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype, fused=fused)
     okc, ovc = H.oracle_caches(case)
     assert np.array_equal(cache_bits(kc), okc), "K cache differs from oracle " + what
     assert np.array_equal(cache_bits(vc), ovc), "V cache differs from oracle " + what
@@ -108,6 +108,7 @@ def test_copy_blocks_copies_whole_blocks():
 
 # ------------------------------------------------------------- configs
 
+@pytest.mark.parametrize("fused", [False, True], ids=["append+attend", "fused_step"])
 @pytest.mark.parametrize("cfg,override", [
     ("1", None),
     ("2", {"B": 3}),                       # 3 x 8193 tokens: many splits + ragged tail
@@ -116,20 +117,20 @@ def test_copy_blocks_copies_whole_blocks():
     ("5a", {"B": 3}),                      # E4M3 cache
     ("5b", {"B": 2}),                      # MHA, G = 1
 ])
-def test_config_shapes_full_compare(cfg, override):
+def test_config_shapes_full_compare(cfg, override, fused):
     case = workloads.make_case(cfg, override=override)
-    err = check_case(case, what="config %s %s" % (cfg, override))
-    print("config %s %s: max abs err %.3g" % (cfg, override, err))
+    err = check_case(case, what="config %s %s" % (cfg, override), fused=fused)
+    print("config %s %s fused=%s: max abs err %.3g" % (cfg, override, fused, err))
 
 
 @pytest.mark.parametrize("cfg,nsample", [("2", 24), ("3", 24), ("4", 8), ("5a", 24), ("5b", 24)])
 def test_config_full_size_sampled(cfg, nsample):
-    """Full-size configuration in the benchmark's launch configuration; the
-    oracle computes a seeded sample of (sequence, KV head) pairs, the caches
-    are compared in full."""
+    """Full-size configuration in the benchmark's launch configuration (the
+    fused step); the oracle computes a seeded sample of (sequence, KV head)
+    pairs, the caches are compared in full."""
     case = workloads.make_case(cfg)
     sel = H.sample_pairs(case, nsample, seed=int(cfg[0]))
-    err = check_case(case, pair_select=sel, what="config %s full size" % cfg)
+    err = check_case(case, pair_select=sel, what="config %s full size" % cfg, fused=True)
     print("config %s full size: max abs err %.3g over %d pairs" % (cfg, err, int(sel.sum())))
 
 
@@ -154,6 +155,7 @@ def test_edge_lengths(D, G, kv_dtype):
     case = workloads.make_custom(len(EDGE_LENS), G * Hkv, Hkv, D, EDGE_LENS, kv_dtype=kv_dtype,
                                  seed=D + G)
     check_case(case, what="D%d G%d dt%d" % (D, G, kv_dtype))
+    check_case(case, what="fused D%d G%d dt%d" % (D, G, kv_dtype), fused=True)
 
 
 def test_group_sizes_two_three_five_seven():
@@ -321,3 +323,52 @@ def test_bad_inputs_are_flagged_not_faulted():
     # the context is still healthy
     x = torch.ones(4, device="cuda") * 2
     assert float(x.sum()) == 8.0
+
+
+def test_workspace_needs_no_initialisation():
+    """Garbage-filled workspace, then the same workspace reused: the in-kernel
+    merge counters must start from zero arrivals each launch."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(5, 32, 8, 128, [3000, 9000, 17, 20000, 513], seed=44)
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, device="cuda", generator=g))
+    out1, kc, vc = H.gpu_step(case, workspace=ws)
+    okc, ovc = H.oracle_caches(case)
+    ref = H.oracle_step(case, okc, ovc)
+    H.compare(case, out1, ref, what="garbage workspace")
+    out2 = torch.empty_like(out1)
+    for _ in range(3):
+        pk.paged_decode_attention(out2, case.q.cuda(), kc, vc,
+                                  torch.from_numpy(case.block_tables).cuda(),
+                                  torch.from_numpy(case.context_lens).cuda(), case.scale, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_fused_step_replays_in_a_cuda_graph():
+    """A captured fused step keeps one counter epoch for every replay; each
+    replay must still merge correctly (the append rewrites the same token)."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(4, 32, 8, 128, [5000, 70, 12000, 4097], seed=45)
+    out_ref, kc, vc = H.gpu_step(case, fused=True)          # first call: per-device set-up
+    q = case.q.cuda()
+    kn, vn = case.k_new.cuda(), case.v_new.cuda()
+    bt = torch.from_numpy(case.block_tables).cuda()
+    cl = torch.from_numpy(case.context_lens).cuda()
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    out = torch.empty_like(out_ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pk.paged_decode_step(out, q, kn, vn, kc, vc, bt, cl, case.scale, ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        pk.paged_decode_step(out, q, kn, vn, kc, vc, bt, cl, case.scale, ws, stream=s)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out_ref.view(torch.int16))
