@@ -60,6 +60,12 @@ namespace pkv {
 __device__ DevErr g_decode_err;
 
 constexpr int kWarps = 4;                        // warps per CTA (independent pipelines)
+// Shared memory given to each warp's ring of stages, and the CTAs per SM the
+// register allocation must allow, per KV element type.
+constexpr int kWarpStageBytesBf16 = 24576;
+constexpr int kWarpStageBytesFp8 = 24576;
+constexpr int kMinCtasBf16 = 1;
+constexpr int kMinCtasFp8 = 1;
 constexpr int kMinBlocksPerWarp = 16;            // do not split below 256 tokens per warp
 constexpr long long kWaitLimit = 1LL << 31;      // ~1 s of SM clocks
 
@@ -72,7 +78,8 @@ struct Geom {
     static constexpr int BOXB = kBlock * BOXW;                // bytes per box
     static constexpr int TILE = kBlock * ROWB;                // one (block, head) tile
     static constexpr int STAGE = 2 * TILE;                    // K + V
-    static constexpr int STAGES_RAW = 24576 / STAGE;
+    static constexpr int STAGES_RAW = (FP8 ? kWarpStageBytesFp8 : kWarpStageBytesBf16) / STAGE;
+    static constexpr int MIN_CTAS = FP8 ? kMinCtasFp8 : kMinCtasBf16;
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
     static constexpr int SWZ = BOXW == 128 ? 7 : 3;           // 128B or 64B swizzle
     static constexpr int KSTEPS = D / 16;
@@ -173,10 +180,17 @@ __device__ __forceinline__ void fill_window(Win& e, const DecodeParams& p, int s
     e.s = s; e.h = h; e.blk = blk; e.L = L;
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
+// Four E4M3 codes (bytes 0..3 of w) -> two f16x2: lo = (byte0, byte1), hi =
+// (byte2, byte3), each element exact (E4M3 is a subset of f16).  The word
+// is split into its 16-bit halves so each conversion reads a register half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Row d of the O^T accumulator held in fragment element (m-tile i, half).
@@ -288,12 +302,13 @@ __device__ __forceinline__ void block_fp8(uint32_t kbase, uint32_t vbase, int nv
     for (int c = 0; c < G::KSTEPS; c += 2) {
         uint32_t r[4];
         ldsm_x4(r, kbase + tile_off<G>(tok, c + csel));
-        mma_f16(sc0, qa0[c], 0u, qa2[c], 0u, e4m3x2_to_f16x2(r[0]), e4m3x2_to_f16x2(r[0] >> 16));
-        mma_f16(sc1, qa0[c], 0u, qa2[c], 0u, e4m3x2_to_f16x2(r[1]), e4m3x2_to_f16x2(r[1] >> 16));
-        mma_f16(sc0, qa0[c + 1], 0u, qa2[c + 1], 0u, e4m3x2_to_f16x2(r[2]),
-                e4m3x2_to_f16x2(r[2] >> 16));
-        mma_f16(sc1, qa0[c + 1], 0u, qa2[c + 1], 0u, e4m3x2_to_f16x2(r[3]),
-                e4m3x2_to_f16x2(r[3] >> 16));
+        uint32_t b[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e4m3x4_to_f16x2x2(r[j], b[j][0], b[j][1]);
+        mma_f16(sc0, qa0[c], 0u, qa2[c], 0u, b[0][0], b[0][1]);
+        mma_f16(sc1, qa0[c], 0u, qa2[c], 0u, b[1][0], b[1][1]);
+        mma_f16(sc0, qa0[c + 1], 0u, qa2[c + 1], 0u, b[2][0], b[2][1]);
+        mma_f16(sc1, qa0[c + 1], 0u, qa2[c + 1], 0u, b[3][0], b[3][1]);
     }
     float pr[4];
     softmax_update<D>(sc0, sc1, nvalid, sl2, m, l, o, pr, lane);
@@ -329,10 +344,10 @@ __device__ __forceinline__ void block_fp8(uint32_t kbase, uint32_t vbase, int nv
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const uint32_t sel = e ? 0x7362u : 0x5140u;
-            const uint32_t u01 = __byte_perm(x[0][w], x[1][w], sel);
-            const uint32_t u23 = __byte_perm(x[2][w], x[3][w], sel);
-            mma_f16(o[2 * w + e], e4m3x2_to_f16x2(u01), e4m3x2_to_f16x2(u01 >> 16),
-                    e4m3x2_to_f16x2(u23), e4m3x2_to_f16x2(u23 >> 16), pf0, pf1);
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(__byte_perm(x[0][w], x[1][w], sel), a[0], a[1]);
+            e4m3x4_to_f16x2x2(__byte_perm(x[2][w], x[3][w], sel), a[2], a[3]);
+            mma_f16(o[2 * w + e], a[0], a[1], a[2], a[3], pf0, pf1);
         }
     }
 }
@@ -481,7 +496,7 @@ __device__ __forceinline__ void append_patch(const DecodeParams& p, int s, int h
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, Geom<D, FP8>::MIN_CTAS)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
 {
@@ -636,6 +651,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     float o[D / 16][4];
     float m = -INFINITY, l = 0.f;
     int seg_s = -1, seg_h = -1, seg_first = 0, seg_last = 0, seg_L = 0, seg_i0 = 0;
+    int seg_pair = -1;
     int st = 0;
     uint32_t phase = 0;
     for (int i = 0; i < cnt; ++i) {
@@ -658,8 +674,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int4 mt = meta[st];
         const bool valid = mt.x >= 0;
         const int pair = valid ? mt.x : -1 - mt.x;
-        const int s = pair / p.Hkv, h = pair - s * p.Hkv, blk = mt.y, L = mt.z;
-        if (s != seg_s || h != seg_h) {
+        const int blk = mt.y, L = mt.z;
+        if (pair != seg_pair) {
+            seg_pair = pair;
+            const int s = pair / p.Hkv, h = pair - s * p.Hkv;
             if (seg_s >= 0)
                 finalize<D, FP8>(p, w, q, seg_s, seg_h, seg_first, seg_last, seg_L, b0 + seg_i0,
                                  m, l, o, lane);
@@ -675,7 +693,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int nvalid = min(kBlock, L - blk * kBlock);
             const uint32_t kb = stage0 + (uint32_t)(st * G::STAGE);
             if (p.k_new != nullptr && nvalid == L - blk * kBlock)     // the pair's last block
-                append_patch<D, FP8>(p, s, h, mt.w, L, kb, kb + G::TILE, lane);
+                append_patch<D, FP8>(p, seg_s, seg_h, mt.w, L, kb, kb + G::TILE, lane);
             if (FP8) block_fp8<D>(kb, kb + G::TILE, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
             else block_bf16<D>(kb, kb + G::TILE, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
         }
