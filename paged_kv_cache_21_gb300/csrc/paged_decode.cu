@@ -85,7 +85,14 @@ struct Geom {
     static constexpr int KSTEPS = D / 16;
     static constexpr int MTILES = D / 16;
     static constexpr int CHUNKS_PER_BOXROW = BOXW / 16;
-    static constexpr int SMEM = kWarps * STAGES * (STAGE + 8 + 16) + 1024;
+    // shared memory: [stages of every warp][mbarriers][stage metadata (int4)],
+    // the stage area aligned to 1024 bytes for the swizzled bulk copies
+    static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
+    static constexpr int META_OFF = (BAR_OFF + kWarps * STAGES * 8 + 15) / 16 * 16;
+    static constexpr int SMEM = META_OFF + kWarps * STAGES * 16 + 1024;
+    static_assert(TILE % 1024 == 0 && BOXB % 512 == 0, "swizzled tiles need aligned stages");
+    static_assert(BAR_OFF % 8 == 0 && META_OFF % 16 == 0, "barrier / metadata alignment");
+    static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // Byte offset inside a tile of 16-byte chunk `c` of token row `r`, after the
@@ -510,9 +517,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (sbase - sraw);
     const uint32_t stage0 = sbase + (uint32_t)(warp * ST * G::STAGE);
-    const uint32_t bar0 = sbase + (uint32_t)(kWarps * ST * G::STAGE + warp * ST * 8);
-    int4* meta = reinterpret_cast<int4*>(gbase + kWarps * ST * G::STAGE + kWarps * ST * 8) +
-                 warp * ST;
+    const uint32_t bar0 = sbase + (uint32_t)(G::BAR_OFF + warp * ST * 8);
+    int4* meta = reinterpret_cast<int4*>(gbase + G::META_OFF) + warp * ST;
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tm_k);
@@ -629,13 +635,17 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, (uint32_t)G::STAGE);
                 const int z = id * p.Hkv + h;
+                // KV tiles are read once per step: keep them from evicting
+                // the block tables, queries and partials from L2
+                const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
                 for (int b = 0; b < G::NBOX; ++b)
-                    tma_load_3d(dst + b * G::BOXB, &tm_k, b * (G::BOXW / G::ES), 0, z, bar);
+                    tma_load_3d_hint(dst + b * G::BOXB, &tm_k, b * (G::BOXW / G::ES), 0, z, bar,
+                                     pol);
 #pragma unroll
                 for (int b = 0; b < G::NBOX; ++b)
-                    tma_load_3d(dst + G::TILE + b * G::BOXB, &tm_v, b * (G::BOXW / G::ES), 0, z,
-                                bar);
+                    tma_load_3d_hint(dst + G::TILE + b * G::BOXB, &tm_v, b * (G::BOXW / G::ES), 0,
+                                     z, bar, pol);
             } else {
                 raise_flag(&g_decode_err, KV_DEVERR_BLOCK_OUT_OF_RANGE, id);
                 mbar_arrive(bar);
