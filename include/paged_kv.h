@@ -135,6 +135,19 @@ int kv_step(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* slot_mapping,
             int32_t* block_tables, int max_blocks, int32_t* context_lens, int32_t* cow_src,
             int32_t* cow_dst, int cow_cap, int* n_cow);
 
+/* Reorder the KV state of a batch of live sequences (beam search selection
+ * or batch-row reuse): after the call, sequence seq_ids[i] holds the length
+ * and blocks that sequence seq_ids[src_index[i]] held before it, e.g. rows
+ * [A0, A1, B0] with src_index [2, 1, 0] become [B0, A1, A0] ("Transformer
+ * attention mask and KV cache inference", section "Batch and beam reorder":
+ * the cache must follow the same permutation as the rows).  With paging this
+ * moves no K/V data: block tables are permuted and shared through reference
+ * counts, so a src_index with repeats (beam duplication) makes the duplicates
+ * share every block, and the next kv_step copies a shared tail block before
+ * appending.  Blocks no row keeps return to the free list.  seq_ids must be
+ * distinct and live; 0 <= src_index[i] < n; on an error nothing changes. */
+int kv_seq_reorder(kv_alloc_t* a, const int64_t* seq_ids, const int32_t* src_index, int n);
+
 /* Read a sequence's state: *len (may be NULL), and its block ids into
  * row[max_blocks] (may be NULL; -1 padded).  *nblocks (may be NULL) gets
  * the number of blocks it holds.  KV_ERR_INVALID_ARG if row is too short. */

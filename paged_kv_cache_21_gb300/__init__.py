@@ -71,6 +71,7 @@ _SIGS = {
     "kv_seq_fork": (_i, [_p, _i64, _i64, _i64]),
     "kv_seq_free": (_i, [_p, _i64]),
     "kv_step": (_i, [_p, _p, _i, _p, _p, _i, _p, _p, _p, _i, ctypes.POINTER(_i)]),
+    "kv_seq_reorder": (_i, [_p, _p, _p, _i]),
     "kv_seq_info": (_i, [_p, _i64, ctypes.POINTER(_i64), _p, _i, ctypes.POINTER(_i)]),
     "kv_alloc_stats": (_i, [_p, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i), _i,
                             ctypes.POINTER(_i)]),
@@ -203,6 +204,15 @@ class BlockAllocator:
                             _np_ptr(lens), _np_ptr(src), _np_ptr(dst), cap, ctypes.byref(ncow)),
                "kv_step")
         return slots, bt, lens, (src[:ncow.value].copy(), dst[:ncow.value].copy())
+
+    def reorder(self, seq_ids, src_index):
+        """Row i of seq_ids takes the KV state row src_index[i] had (beam
+        reorder / duplication; block tables only, reference counted)."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        src = np.ascontiguousarray(src_index, dtype=np.int32)
+        assert ids.shape == src.shape
+        _check(_lib.kv_seq_reorder(self._h, _np_ptr(ids), _np_ptr(src), ids.shape[0]),
+               "kv_seq_reorder")
 
     def info(self, seq_id, max_blocks=None):
         """(length, block ids) of a sequence."""

@@ -195,6 +195,32 @@ int kv_step(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* slot_mapping,
     return KV_OK;
 }
 
+int kv_seq_reorder(kv_alloc_t* a, const int64_t* seq_ids, const int32_t* src_index, int n)
+{
+    if (!a || n < 0) return KV_ERR_INVALID_ARG;
+    if (n == 0) return KV_OK;
+    if (!seq_ids || !src_index) return KV_ERR_INVALID_ARG;
+    std::unordered_set<int64_t> seen;
+    std::vector<Seq*> rows(n);
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return KV_ERR_NOT_FOUND;
+        if (!seen.insert(seq_ids[i]).second) return KV_ERR_INVALID_ARG;
+        if (src_index[i] < 0 || src_index[i] >= n) return KV_ERR_INVALID_ARG;
+        rows[i] = &it->second;
+    }
+    // snapshot, then take the new references before dropping the old ones so
+    // that a block kept by some row never visits the free list
+    std::vector<Seq> old(n);
+    for (int i = 0; i < n; ++i) old[i] = *rows[i];
+    for (int i = 0; i < n; ++i)
+        for (int32_t b : old[src_index[i]].blocks) a->refcount[b] += 1;
+    for (int i = 0; i < n; ++i)
+        for (int32_t b : old[i].blocks) a->release(b);
+    for (int i = 0; i < n; ++i) *rows[i] = old[src_index[i]];
+    return KV_OK;
+}
+
 int kv_seq_info(kv_alloc_t* a, int64_t seq_id, int64_t* len, int32_t* row, int max_blocks,
                 int* nblocks)
 {

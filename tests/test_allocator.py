@@ -177,3 +177,36 @@ def test_random_operations_keep_pool_invariants(pk):
     for b in range(NB):
         assert a.stats(b)[3] == holders.get(b, 0)
     assert a.stats()[1] == len(holders)
+
+
+def test_reorder_follows_the_row_permutation(pk):
+    # rows [A0, A1, B0] -> [B0, A1, A0]: permutation [2, 1, 0]
+    a = pk.BlockAllocator(32, 1, 64)
+    a.add(10, 20)      # A0
+    a.add(11, 35)      # A1
+    a.add(12, 50)      # B0
+    before = {sid: a.info(sid) for sid in (10, 11, 12)}
+    a.reorder([10, 11, 12], [2, 1, 0])
+    assert a.info(10)[0] == before[12][0] and list(a.info(10)[1]) == list(before[12][1])
+    assert a.info(11)[0] == before[11][0] and list(a.info(11)[1]) == list(before[11][1])
+    assert a.info(12)[0] == before[10][0] and list(a.info(12)[1]) == list(before[10][1])
+    assert a.stats()[:3] == (32 - 2 - 3 - 4, 9, 3)
+
+
+def test_reorder_with_duplicates_shares_and_releases(pk):
+    a = pk.BlockAllocator(32, 1, 64)
+    a.add(0, 40)                                 # 3 blocks, tail partial
+    a.add(1, 17)                                 # 2 blocks
+    b0 = a.info(0)[1]
+    a.reorder([0, 1], [0, 0])                    # beam 1 becomes a copy of beam 0
+    assert list(a.info(1)[1]) == list(b0) and a.info(1)[0] == 40
+    assert a.stats()[1] == 3                     # beam 1's old blocks went back to the pool
+    for b in b0:
+        assert a.stats(int(b))[3] == 2
+    slots, bt, lens, (cs, cd) = a.step([0, 1], 8)
+    assert list(cs) == [b0[2]] and len(cd) == 1  # the shared tail is copied once
+    assert bt[0, 2] != bt[1, 2]
+    with pytest.raises(pk.KVError):
+        a.reorder([0, 1], [0, 2])                # index out of range
+    with pytest.raises(pk.KVError):
+        a.reorder([0, 0], [0, 1])                # repeated sequence id

@@ -372,3 +372,61 @@ def test_fused_step_replays_in_a_cuda_graph():
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), out_ref.view(torch.int16))
+
+
+def test_beam_reorder_and_duplication_through_the_kernels():
+    """Rows [A0, A1, B0] reordered by [2, 1, 0], then beams duplicated by
+    [0, 0, 1] (copy-on-write at the next append), with decode steps in
+    between; every step is checked against the oracle on the same tables."""
+    import paged_kv_cache_21_gb300 as pk
+    Hq, Hkv, D, NB, MB = 8, 2, 128, 64, 8
+    alloc = pk.BlockAllocator(NB, Hkv, D)
+    g = torch.Generator().manual_seed(77)
+    kc = torch.zeros((NB, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    okc = np.zeros((NB, Hkv, 16, D), dtype=np.uint16)
+    ovc = np.zeros_like(okc)
+    ids = [10, 11, 12]
+    for sid, L in zip(ids, (21, 37, 50)):
+        alloc.add(sid, L)
+        _, row = alloc.info(sid)
+        kk = torch.randn((L, Hkv, D), generator=g).to(torch.bfloat16)
+        vv = torch.randn((L, Hkv, D), generator=g).to(torch.bfloat16)
+        sl = np.array([row[p // 16] * 16 + p % 16 for p in range(L)], dtype=np.int64)
+        pk.kv_append(kk.cuda(), vv.cuda(), kc, vc, torch.from_numpy(sl).cuda())
+        oracle.append(okc, ovc, bf16_bits(kk), bf16_bits(vv), sl, oracle.BF16)
+    ws = pk.alloc_workspace(3, Hq, Hkv, D)
+
+    def step(expect_lens=None):
+        slots, bt, lens, (cs, cd) = alloc.step(ids, MB)
+        if expect_lens is not None:
+            assert list(lens) == expect_lens
+        if len(cs):
+            pk.kv_copy_blocks(kc, vc, torch.from_numpy(cs).cuda(), torch.from_numpy(cd).cuda())
+            for s_, d_ in zip(cs, cd):
+                okc[d_] = okc[s_]
+                ovc[d_] = ovc[s_]
+        k = torch.randn((3, Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((3, Hkv, D), generator=g).to(torch.bfloat16)
+        q = torch.randn((3, Hq, D), generator=g).to(torch.bfloat16)
+        out = torch.empty((3, Hq, D), dtype=torch.float32, device="cuda")
+        pk.paged_decode_step(out, q.cuda(), k.cuda(), v.cuda(), kc, vc,
+                             torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda(),
+                             1 / math.sqrt(D), ws)
+        oracle.append(okc, ovc, bf16_bits(k), bf16_bits(v), slots, oracle.BF16)
+        ref = oracle.paged_attention(oracle.bf16_bits_to_f64(bf16_bits(q)), okc, ovc, bt, lens,
+                                     1 / math.sqrt(D))
+        torch.cuda.synchronize()
+        assert np.array_equal(cache_bits(kc), okc)
+        assert np.max(np.abs(out.cpu().numpy() - ref)) < 2e-3
+        return lens
+
+    step([22, 38, 51])
+    alloc.reorder(ids, [2, 1, 0])          # [A0, A1, B0] -> [B0, A1, A0]
+    step([52, 39, 23])
+    alloc.reorder(ids, [0, 0, 1])          # beam duplication: rows 0 and 1 share B0's history
+    for _ in range(20):
+        step()
+    for sid in ids:
+        alloc.free(sid)
+    assert alloc.stats()[0] == NB
