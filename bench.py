@@ -34,9 +34,11 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "33a8bf28d1f6c11e3ec12195d848e56dcccf62e87e6a1fd2174788a48455755f",
-           "bytes_per_launch": 1092060000,
-           "source": "ncu batch-8 capture scaled x4 by units (profiles/paged_decode_split_b8_full.md)"}
+TRAFFIC = {"kernel_sha256": "10231aca36ee01944cb68a90e66f45dd1ca79051fe31c425abfe49980849d5b6",
+           "bytes_per_launch": 1088440000,
+           "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
+                     "(269.14 MB + 2.97 MB), scaled x4 by units processed "
+                     "(profiles/paged_decode_split_b8_full.md)"}
 
 
 def parse_args(argv=None):
