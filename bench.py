@@ -330,9 +330,10 @@ def run_ours(args):
         pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
                                         case.k_scale, case.v_scale, stream=stream)
 
-    def timed(K, body, nev):
+    def timed(K, body, nev, tail=None):
         """Run exactly K steps between a barrier + sync on both sides; events
-        ev[i][0..nev-1] are handed to the body of step i."""
+        ev[i][0..nev-1] are handed to the body of step i; `tail` runs before
+        the end event is recorded (to join work on other streams)."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
         for e in ev:                  # create the event handles before the timed region
             for x in e:
@@ -345,6 +346,8 @@ def run_ours(args):
         t_beg.record(stream)
         for i in range(K):
             body(ev[i])
+        if tail is not None:
+            tail()
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -395,37 +398,38 @@ def run_ours(args):
                "merge_us": statistics.mean(un_ev[i][2].elapsed_time(un_ev[i][3])
                                            for i in range(K)) * 1e3}
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs (pinned), the fused step, D2H of the output, every step
+    # end to end through the public API with host buffers: every step copies
+    # its inputs (staged in one pinned buffer) to the device, runs the fused
+    # step and copies its output back; the copies run on a copy stream with
+    # two alternating staging slots, overlapping the neighbouring steps
     e2e = None
     if not args.no_e2e:
-        h_q = q.cpu().pin_memory()
-        h_k = k_new.cpu().pin_memory()
-        h_v = v_new.cpu().pin_memory()
-        h_bt = torch.from_numpy(case.block_tables).pin_memory()
-        h_cl = torch.from_numpy(case.context_lens).pin_memory()
-        h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
-        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-        d_bt, d_cl = torch.empty_like(bt), torch.empty_like(cl)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_cl))
-        d2h = h_out.numel() * h_out.element_size()
+        stg = pk.DecodeStepStaging(B, Hq, Hkv, D, case.max_blocks, case.kv_dtype, device=device)
+        for j in range(2):
+            hs = stg.host(j)
+            hs.q.copy_(q.cpu())
+            hs.k_new.copy_(k_new.cpu())
+            hs.v_new.copy_(v_new.cpu())
+            hs.block_tables.copy_(torch.from_numpy(case.block_tables))
+            hs.context_lens.copy_(torch.from_numpy(case.context_lens))
+        counter = [0]
 
         def e2e_step(_e=None):
-            d_q.copy_(h_q, non_blocking=True)
-            d_k.copy_(h_k, non_blocking=True)
-            d_v.copy_(h_v, non_blocking=True)
-            d_bt.copy_(h_bt, non_blocking=True)
-            d_cl.copy_(h_cl, non_blocking=True)
-            pk.paged_decode_step(out, d_q, d_k, d_v, kc, vc, d_bt, d_cl, case.scale, ws,
-                                 case.k_scale, case.v_scale, stream=stream)
-            h_out.copy_(out, non_blocking=True)
+            stg.step(counter[0], kc, vc, case.scale, case.k_scale, case.v_scale, stream=stream)
+            counter[0] += 1
 
         for _ in range(max(args.warmup, 3)):
             e2e_step()
-        e2e_ms_local, _ = timed(K, e2e_step, 0)
+        torch.cuda.synchronize()
+        # the end event waits for the last download on its copy stream
+        e2e_ms_local, _ = timed(K, e2e_step, 0, tail=lambda: stg.join(stream))
         e2e_ms = reduce_max(e2e_ms_local, world, device)
+        torch.cuda.synchronize()
+        assert torch.equal(stg.host(counter[0] - 1).out.view(torch.int16),
+                           out.cpu().view(torch.int16))
         e2e = {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": stg.h2d_bytes,
+               "d2h_bytes_per_step": stg.d2h_bytes}
 
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9

@@ -345,3 +345,107 @@ def get_device_error():
     d = _i64(0)
     _check(_lib.kv_get_device_error(ctypes.byref(f), ctypes.byref(d)), "kv_get_device_error")
     return f.value, d.value
+
+
+class DecodeStepStaging:
+    """Host-to-device plumbing for a stream of decode steps.
+
+    Each of ``slots`` staging slots is one pinned host buffer holding every
+    per-step input -- q [B, Hq, D] bf16, k_new / v_new [B, Hkv, D] bf16,
+    block_tables [B, max_blocks] int32, context_lens [B] int32 -- at 256-byte
+    aligned offsets, mirrored by one device buffer, plus an output buffer on
+    each side.  A step costs one host-to-device copy, the fused step kernels
+    (paged_decode_step) and one device-to-host copy of the output.  Uploads
+    and downloads run on two copy streams of their own and the slots
+    alternate, so step i+1's upload and step i's download overlap the kernels
+    of the steps around them.
+
+    Use: fill ``host(i)`` views of slot i % slots (``q``, ``k_new``,
+    ``v_new``, ``block_tables``, ``context_lens``) once ``ready_for_input(i)``
+    holds, call ``step(i, ...)``, and read ``host(i).out`` after
+    ``wait_output(i)``."""
+
+    _ALIGN = 256
+
+    class _Slot:
+        pass
+
+    def __init__(self, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                 kv_dtype=BF16, device=None, out_dtype=None, slots=2):
+        import torch
+        self.device = torch.device(device or "cuda")
+        B, Hq, Hkv, D = num_seqs, num_q_heads, num_kv_heads, head_dim
+        parts = [("q", (B, Hq, D), torch.bfloat16), ("k_new", (B, Hkv, D), torch.bfloat16),
+                 ("v_new", (B, Hkv, D), torch.bfloat16),
+                 ("block_tables", (B, max_blocks), torch.int32),
+                 ("context_lens", (B,), torch.int32)]
+        offs, off = {}, 0
+        for name, shape, dt in parts:
+            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+            offs[name] = (off, shape, dt, nbytes)
+            off = -(-(off + nbytes) // self._ALIGN) * self._ALIGN
+        self.nbytes = off
+        od = out_dtype or torch.bfloat16
+        self._slots = []
+        for _ in range(slots):
+            h, d = self._Slot(), self._Slot()
+            h.raw = torch.empty(off, dtype=torch.uint8).pin_memory()
+            d.raw = torch.empty(off, dtype=torch.uint8, device=self.device)
+            for name, (o, shape, dt, nb) in offs.items():
+                setattr(h, name, h.raw[o:o + nb].view(dt).view(shape))
+                setattr(d, name, d.raw[o:o + nb].view(dt).view(shape))
+            h.out = torch.empty((B, Hq, D), dtype=od).pin_memory()
+            d.out = torch.empty((B, Hq, D), dtype=od, device=self.device)
+            ev = {k: torch.cuda.Event() for k in ("uploaded", "computed", "downloaded")}
+            self._slots.append((h, d, ev))
+        self.upload_stream = torch.cuda.Stream(self.device)
+        self.download_stream = torch.cuda.Stream(self.device)
+        self.workspace = alloc_workspace(B, Hq, Hkv, D, kv_dtype, device=self.device)
+
+    def host(self, i):
+        return self._slots[i % len(self._slots)][0]
+
+    @property
+    def h2d_bytes(self):
+        return self.nbytes
+
+    @property
+    def d2h_bytes(self):
+        h = self._slots[0][0]
+        return h.out.numel() * h.out.element_size()
+
+    def ready_for_input(self, i):
+        """Block the host until slot i % slots may be refilled (its previous
+        upload has finished)."""
+        self._slots[i % len(self._slots)][2]["uploaded"].synchronize()
+
+    def wait_output(self, i):
+        self._slots[i % len(self._slots)][2]["downloaded"].synchronize()
+
+    def step(self, i, k_cache, v_cache, scale, k_scale=1.0, v_scale=1.0, stream=None):
+        """Upload slot i's inputs, run the fused decode step on `stream`,
+        download its output (all asynchronous)."""
+        import torch
+        h, d, ev = self._slots[i % len(self._slots)]
+        s = stream or torch.cuda.current_stream(self.device)
+        up, down = self.upload_stream, self.download_stream
+        # the device slot is free once its previous step has been computed
+        up.wait_event(ev["computed"])
+        with torch.cuda.stream(up):
+            d.raw.copy_(h.raw, non_blocking=True)
+            ev["uploaded"].record(up)
+        s.wait_event(ev["uploaded"])
+        paged_decode_step(d.out, d.q, d.k_new, d.v_new, k_cache, v_cache, d.block_tables,
+                          d.context_lens, scale, self.workspace, k_scale, v_scale, stream=s)
+        ev["computed"].record(s)
+        down.wait_event(ev["computed"])
+        with torch.cuda.stream(down):
+            h.out.copy_(d.out, non_blocking=True)
+            ev["downloaded"].record(down)
+
+    def join(self, stream=None):
+        """Make `stream` wait for every upload and download issued so far."""
+        import torch
+        s = stream or torch.cuda.current_stream(self.device)
+        s.wait_stream(self.upload_stream)
+        s.wait_stream(self.download_stream)

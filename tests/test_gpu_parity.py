@@ -430,3 +430,31 @@ def test_beam_reorder_and_duplication_through_the_kernels():
     for sid in ids:
         alloc.free(sid)
     assert alloc.stats()[0] == NB
+
+
+def test_staged_host_steps_match_device_step():
+    """DecodeStepStaging (per step: one H2D copy of every input on a copy
+    stream, fused step, one D2H copy; two alternating slots) gives the same
+    bits as the fused step on device inputs, step after step."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(5, 32, 8, 128, [1, 300, 4097, 9000, 20], seed=81)
+    out_ref, kc, vc = H.gpu_step(case, fused=True)
+    # the fused step already appended the new tokens; rerunning rewrites them identically
+    stg = pk.DecodeStepStaging(case.B, case.Hq, case.Hkv, case.D, case.max_blocks)
+    for i in range(5):
+        stg.ready_for_input(i)
+        hs = stg.host(i)
+        hs.q.copy_(case.q)
+        hs.k_new.copy_(case.k_new)
+        hs.v_new.copy_(case.v_new)
+        hs.block_tables.copy_(torch.from_numpy(case.block_tables))
+        hs.context_lens.copy_(torch.from_numpy(case.context_lens))
+        hs.out.zero_()
+        stg.step(i, kc, vc, case.scale)
+        if i >= 1:
+            stg.wait_output(i - 1)
+            assert torch.equal(stg.host(i - 1).out.view(torch.int16),
+                               out_ref.cpu().view(torch.int16))
+    stg.wait_output(4)
+    assert torch.equal(stg.host(4).out.view(torch.int16), out_ref.cpu().view(torch.int16))
+    assert stg.h2d_bytes >= (5 * 32 * 128 + 2 * 5 * 8 * 128) * 2
