@@ -545,10 +545,19 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         carry = __shfl_sync(kFull, incl[u], 31);
     }
     int total = carry;
-    for (int base = U * 32; base < p.B; base += 32) {
-        const int s = base + lane;
-        int Lc;
-        total += warp_sum(s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) * p.Hkv : 0);
+    // sequences past the first 256: 256 at a time, all loads issued together
+    for (int base = U * 32; base < p.B; base += U * 32) {
+        int v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = base + u * 32 + lane;
+            int Lc;
+            v[u] = s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) : 0;
+        }
+        int sum = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) sum += v[u];
+        total += warp_sum(sum) * p.Hkv;
     }
     if (total == 0) return;
     int q = (total + p.warps_total - 1) / p.warps_total;
@@ -571,19 +580,25 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     if (s0 < 0) {
         int c2 = carry;
-        for (int base = U * 32; base < p.B; base += 32) {
-            const int s = base + lane;
-            int Lc;
-            const int v = s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) * p.Hkv : 0;
-            const int inc = warp_incl_scan(v, lane) + c2;
-            const unsigned mball = __ballot_sync(kFull, inc > b0);
-            if (mball) {
-                const int src = __ffs(mball) - 1;
-                s0 = base + src;
-                excl = __shfl_sync(kFull, inc - v, src);
-                break;
+        for (int base = U * 32; base < p.B && s0 < 0; base += U * 32) {
+            int v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int s = base + u * 32 + lane;
+                int Lc;
+                v[u] = s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) * p.Hkv : 0;
             }
-            c2 = __shfl_sync(kFull, inc, 31);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int inc = warp_incl_scan(v[u], lane) + c2;
+                const unsigned mball = __ballot_sync(kFull, inc > b0);
+                if (s0 < 0 && mball) {
+                    const int src = __ffs(mball) - 1;
+                    s0 = base + u * 32 + src;
+                    excl = __shfl_sync(kFull, inc - v[u], src);
+                }
+                c2 = __shfl_sync(kFull, inc, 31);
+            }
         }
     }
     if (s0 < 0) return;      // unreachable with consistent input

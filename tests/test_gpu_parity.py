@@ -166,9 +166,12 @@ def test_group_sizes_two_three_five_seven():
 
 def test_many_sequences_beyond_register_scan():
     # more than 256 sequences takes the second scan path of the split kernel
-    lens = (np.arange(300) * 37) % 500 + 1
-    case = workloads.make_custom(300, 8, 2, 64, lens, seed=77)
-    check_case(case, what="B=300")
+    # (three chunks of 256 here), with some empty contexts mixed in
+    lens = (np.arange(700) * 37) % 500 + 1
+    case = workloads.make_custom(700, 8, 2, 64, lens, seed=77)
+    case.context_lens[::97] = 0
+    check_case(case, what="B=700")
+    check_case(case, what="B=700 fused", fused=True)
 
 
 def test_empty_contexts_give_zeros():
@@ -458,3 +461,51 @@ def test_staged_host_steps_match_device_step():
     stg.wait_output(4)
     assert torch.equal(stg.host(4).out.view(torch.int16), out_ref.cpu().view(torch.int16))
     assert stg.h2d_bytes >= (5 * 32 * 128 + 2 * 5 * 8 * 128) * 2
+
+
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_token_by_token_decode_equals_causal_prefill(kv_dtype):
+    """Decode two sequences from empty, one token per step through the fused
+    step; step t must equal row t of full causal attention over the same
+    tokens (the mask/KV page's check that prefill and token-by-token decode
+    agree)."""
+    import paged_kv_cache_21_gb300 as pk
+    Hq, Hkv, D, T, NB, MB = 8, 2, 64, 70, 16, 8
+    g = torch.Generator().manual_seed(91 + kv_dtype)
+    Q = torch.randn((2, T, Hq, D), generator=g).to(torch.bfloat16)
+    Kt = torch.randn((2, T, Hkv, D), generator=g).to(torch.bfloat16)
+    Vt = torch.randn((2, T, Hkv, D), generator=g).to(torch.bfloat16)
+    ks = vs = 1.0
+    if kv_dtype == workloads.FP8_E4M3:
+        ks = float(np.float32(float(Kt.abs().max())) / np.float32(448.0))
+        vs = float(np.float32(float(Vt.abs().max())) / np.float32(448.0))
+    alloc = pk.BlockAllocator(NB, Hkv, D, kv_dtype)
+    alloc.add(0, 0)
+    alloc.add(1, 0)
+    cdt = torch.bfloat16 if kv_dtype == workloads.BF16 else torch.uint8
+    kc = torch.zeros((NB, Hkv, 16, D), dtype=cdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    ws = pk.alloc_workspace(2, Hq, Hkv, D, kv_dtype)
+    # the values the cache holds, as the oracle sees them (dequantised for E4M3)
+    if kv_dtype == workloads.FP8_E4M3:
+        Kv = oracle.e4m3_decode_array(oracle.quantize_e4m3(bf16_bits(Kt), ks)) * ks
+        Vv = oracle.e4m3_decode_array(oracle.quantize_e4m3(bf16_bits(Vt), vs)) * vs
+    else:
+        Kv, Vv = oracle.bf16_bits_to_f64(bf16_bits(Kt)), oracle.bf16_bits_to_f64(bf16_bits(Vt))
+    Qv = oracle.bf16_bits_to_f64(bf16_bits(Q))
+    full = np.empty((2, T, Hq, D))
+    for s in range(2):
+        for h in range(Hq):
+            full[s, :, h] = oracle.causal_attention(Qv[s, :, h], Kv[s, :, h // (Hq // Hkv)],
+                                                    Vv[s, :, h // (Hq // Hkv)], 1 / math.sqrt(D))
+    tol = H.tolerance(kv_dtype)
+    for t in range(T):
+        _, bt, lens, (cs, cd) = alloc.step([0, 1], MB)
+        assert len(cs) == 0 and list(lens) == [t + 1, t + 1]
+        out = torch.empty((2, Hq, D), dtype=torch.float32, device="cuda")
+        pk.paged_decode_step(out, Q[:, t].contiguous().cuda(), Kt[:, t].contiguous().cuda(),
+                             Vt[:, t].contiguous().cuda(), kc, vc, torch.from_numpy(bt).cuda(),
+                             torch.from_numpy(lens).cuda(), 1 / math.sqrt(D), ws, ks, vs)
+        torch.cuda.synchronize()
+        err = np.max(np.abs(out.cpu().numpy() - full[:, t]))
+        assert err < tol, (t, err)
