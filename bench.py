@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "10231aca36ee01944cb68a90e66f45dd1ca79051fe31c425abfe49980849d5b6",
-           "bytes_per_launch": 1088440000,
+TRAFFIC = {"kernel_sha256": "11486b326ea9eca93e11e3fccf1698333676049533c1ac37ff56796105c88f12",
+           "bytes_per_launch": 1087536128,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269.14 MB + 2.97 MB), scaled x4 by units processed "
+                     "(269,157,632 B + 2,726,400 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 
