@@ -193,8 +193,9 @@ def oracle_prepare(case):
     return kc, vc, q64, kb, vb
 
 
-def oracle_step(case, prep):
-    """One oracle decode step on the sample: append + attention (float64)."""
+def oracle_step(case, prep, nthreads=0):
+    """One oracle decode step on the sample: append + attention (float64).
+    nthreads 0 = all host cores."""
     import numpy as np
     import oracle
     kc, vc, q64, kb, vb = prep
@@ -203,7 +204,7 @@ def oracle_step(case, prep):
     oracle.append(kc, vc, kb, vb, slots, case.kv_dtype, case.k_scale, case.v_scale)
     return oracle.paged_attention(q64, kc, vc, case.block_tables, case.context_lens, case.scale,
                                   kv_dtype=case.kv_dtype, k_scale=case.k_scale,
-                                  v_scale=case.v_scale)
+                                  v_scale=case.v_scale, nthreads=nthreads)
 
 
 def cpu_baseline(cfg, budget_s, seqs=4):
@@ -219,7 +220,14 @@ def cpu_baseline(cfg, budget_s, seqs=4):
         if el >= budget_s or n >= 10000:
             break
     gbs = case.logical_kv_bytes() * n / el / 1e9
+    # the same sample on one thread (up to 3 steps)
+    n1, t1 = 0, time.perf_counter()
+    while n1 < 3 and time.perf_counter() - t1 < budget_s / 2:
+        oracle_step(case, prep, nthreads=1)
+        n1 += 1
+    gbs1 = case.logical_kv_bytes() * n1 / (time.perf_counter() - t1) / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "value_1_thread": gbs1,
             "sample": "%d of %d sequences of this workload (%d (seq, KV head) pairs, "
                       "%d bytes of KV per step), float64 C oracle with OpenMP, %d steps in %.1f s"
                       % (case.B, 32 if cfg in ("2", "5a") else case.B, case.B * case.Hkv,
@@ -431,6 +439,22 @@ def run_ours(args):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": stg.h2d_bytes,
                "d2h_bytes_per_step": stg.d2h_bytes}
 
+    # same-run copy ceiling: a plain device-to-device copy of 1 GiB (read + write bytes)
+    src = torch.ones(1 << 29, dtype=torch.int16, device=device)
+    dst = torch.empty_like(src)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dst.copy_(src)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(10):
+            dst.copy_(src)
+        r1.record(stream)
+    torch.cuda.synchronize()
+    copy_ceiling = {"gbs": 10 * 2 * src.numel() * 2 / (r0.elapsed_time(r1) * 1e-3) / 1e9,
+                    "how": "torch copy_ of a 1 GiB buffer, read + write bytes, same run"}
+    del src, dst
+
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256"] == kernel_sha() else None
@@ -441,7 +465,8 @@ def run_ours(args):
                 "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
-                "split_us": split_ms * 1e3, "merge_us": merge_ms * 1e3}
+                "split_us": split_ms * 1e3, "merge_us": merge_ms * 1e3,
+                "copy_ceiling": copy_ceiling}
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": ms,

@@ -290,8 +290,9 @@ int orc_paged_attention(double* out, const double* q, const uint8_t* k_cache,
     int npairs = num_seqs * num_kv_heads;
     int rc = 0;
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(min : rc)
+    /* a per-call team size; the process-wide default stays as it was */
+    const int team = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel for num_threads(team) schedule(dynamic, 1) reduction(min : rc)
 #endif
     for (int p = 0; p < npairs; ++p) {
         if (pair_select && !pair_select[p]) continue;
