@@ -394,6 +394,36 @@ def run_ours(args):
     split_ms = statistics.mean(sp_ev[i][0].elapsed_time(sp_ev[i][1]) for i in range(K))
     merge_ms = statistics.mean(sp_ev[i][1].elapsed_time(sp_ev[i][2]) for i in range(K))
 
+    # one fused step captured in a CUDA graph and replayed, each replay
+    # bracketed by events: the median is the per-layer-step latency
+    gs = torch.cuda.Stream(device)
+    gs.wait_stream(stream)
+    with torch.cuda.stream(gs):
+        pk.paged_decode_step(out, q, k_new, v_new, kc, vc, bt, cl, case.scale, ws,
+                             case.k_scale, case.v_scale, stream=gs)
+    stream.wait_stream(gs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        pk.paged_decode_step(out, q, k_new, v_new, kc, vc, bt, cl, case.scale, ws,
+                             case.k_scale, case.v_scale, stream=gs)
+    n_rep = max(K, 100)
+    g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_rep)]
+    with torch.cuda.stream(gs):
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+        for a, b in g_ev:
+            a.record(gs)
+            graph.replay()
+            b.record(gs)
+    torch.cuda.synchronize()
+    g_us = sorted(a.elapsed_time(b) * 1e3 for a, b in g_ev)
+    graph_replay = {"median_us": statistics.median(g_us), "min_us": g_us[0],
+                    "p90_us": g_us[int(0.9 * (len(g_us) - 1))], "replays": n_rep,
+                    "kv_gbs_at_median": kv_bytes / (statistics.median(g_us) * 1e-6) / 1e9}
+    del graph
+
     # the same step as separate launches (kv_append, then paged_decode_attention)
     for _ in range(max(args.warmup, 3)):
         step_unfused([None, None, None])
@@ -479,7 +509,7 @@ def run_ours(args):
             "config": dict(workload_config(cfg),
                            parallelism="replicas x%d" % world if world > 1 else "single GPU"),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
-            "unfused": unfused}
+            "unfused": unfused, "graph_replay": graph_replay}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     if rank == 0:
