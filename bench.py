@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "11486b326ea9eca93e11e3fccf1698333676049533c1ac37ff56796105c88f12",
-           "bytes_per_launch": 1087536128,
+TRAFFIC = {"kernel_sha256": "375a4c1dd6128210d7ceb15c99105e866319bc0aaa2ef502b1f86c1c6d9f94c3",
+           "bytes_per_launch": 1089233920,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,157,632 B + 2,726,400 B), scaled x4 by units processed "
+                     "(269,179,392 B + 3,129,088 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 
@@ -261,7 +261,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(args.config),
+            "data": "synthetic", "config": workload_config(args.config, args.batch),
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "kind": "oracle",
                              "cores": oracle.max_threads(), "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -270,10 +270,12 @@ def run_reference(args):
     return 0
 
 
-def workload_config(cfg):
+def workload_config(cfg, batch=None):
     """The workload description shared by both arms (from the recipe only)."""
     import workloads
-    spec = workloads.CONFIGS[cfg]
+    spec = dict(workloads.CONFIGS[cfg])
+    if batch:
+        spec["B"] = batch
     es = 1 if spec["kv_dtype"] == workloads.FP8_E4M3 else 2
     c = {"workload": spec["desc"], "config_id": cfg, "batch": spec["B"],
          "q_heads": spec["Hq"], "kv_heads": spec["Hkv"], "head_dim": spec["D"],
@@ -487,7 +489,10 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256"] == kernel_sha() else None
+    # the recorded counters belong to the default workload (config 2, batch 32)
+    traffic = (TRAFFIC["bytes_per_launch"]
+               if TRAFFIC["kernel_sha256"] == kernel_sha() and cfg == "2" and not args.batch
+               else None)
     roofline = {"bound": "hbm",
                 "kernel": "paged_decode_split_kernel<%d,%s>" % (
                     D, "bf16" if case.kv_dtype == workloads.BF16 else "e4m3"),
@@ -506,7 +511,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if case.kv_dtype == workloads.BF16 else "e4m3",
             "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
-            "config": dict(workload_config(cfg),
+            "config": dict(workload_config(cfg, args.batch),
                            parallelism="replicas x%d" % world if world > 1 else "single GPU"),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
             "unfused": unfused, "graph_replay": graph_replay}

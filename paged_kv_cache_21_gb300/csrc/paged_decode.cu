@@ -210,33 +210,50 @@ __device__ __forceinline__ int out_dim(int i, int g, int half)
 
 // ------------------------------------------------------------ per-block math
 
-// Scores of the 16 tokens of one block for this lane's head (lane / 4) and
-// the online-softmax update; returns the probabilities of tokens
-// (2t, 2t+1, 2t+8, 2t+9) and rescales the accumulator.
-template <int D>
-__device__ __forceinline__ void softmax_update(const float (&sc0)[4], const float (&sc1)[4],
-                                               int nvalid, float sl2, float& m, float& l,
-                                               float (&o)[D / 16][4], float (&pr)[4], int lane)
+// Online-softmax update over NBK consecutive blocks of one pair, from each
+// block's scores of this lane's head (lane / 4) at tokens (2t, 2t+1, 2t+8,
+// 2t+9); only the last block may be partial (nvalid_last tokens).  Returns
+// the probabilities of those tokens and rescales the accumulator.
+template <int D, int NBK>
+__device__ __forceinline__ void softmax_update(const float (&sc)[NBK][2][4], int nvalid_last,
+                                               float sl2, float& m, float& l,
+                                               float (&o)[D / 16][4], float (&pr)[NBK][4],
+                                               int lane)
 {
     const int t = lane & 3;
-    float x0 = sc0[0] * sl2, x1 = sc0[1] * sl2, x2 = sc1[0] * sl2, x3 = sc1[1] * sl2;
-    if (nvalid < kBlock) {
-        const int t0 = 2 * t;
-        if (t0 >= nvalid) x0 = -INFINITY;
-        if (t0 + 1 >= nvalid) x1 = -INFINITY;
-        if (t0 + 8 >= nvalid) x2 = -INFINITY;
-        if (t0 + 9 >= nvalid) x3 = -INFINITY;
+    float x[NBK][4];
+#pragma unroll
+    for (int j = 0; j < NBK; ++j) {
+        x[j][0] = sc[j][0][0] * sl2;
+        x[j][1] = sc[j][0][1] * sl2;
+        x[j][2] = sc[j][1][0] * sl2;
+        x[j][3] = sc[j][1][1] * sl2;
     }
-    float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    if (nvalid_last < kBlock) {
+        const int t0 = 2 * t;
+        if (t0 >= nvalid_last) x[NBK - 1][0] = -INFINITY;
+        if (t0 + 1 >= nvalid_last) x[NBK - 1][1] = -INFINITY;
+        if (t0 + 8 >= nvalid_last) x[NBK - 1][2] = -INFINITY;
+        if (t0 + 9 >= nvalid_last) x[NBK - 1][3] = -INFINITY;
+    }
+    float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
+#pragma unroll
+    for (int j = 1; j < NBK; ++j)
+        mx = fmaxf(mx, fmaxf(fmaxf(x[j][0], x[j][1]), fmaxf(x[j][2], x[j][3])));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
     const float m_new = fmaxf(m, mx);
     const float alpha = exp2f(m - m_new);
-    pr[0] = exp2f(x0 - m_new);
-    pr[1] = exp2f(x1 - m_new);
-    pr[2] = exp2f(x2 - m_new);
-    pr[3] = exp2f(x3 - m_new);
-    l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NBK; ++j) {
+        pr[j][0] = exp2f(x[j][0] - m_new);
+        pr[j][1] = exp2f(x[j][1] - m_new);
+        pr[j][2] = exp2f(x[j][2] - m_new);
+        pr[j][3] = exp2f(x[j][3] - m_new);
+        sum += (pr[j][0] + pr[j][1]) + (pr[j][2] + pr[j][3]);
+    }
+    l = l * alpha + sum;
     m = m_new;
     // accumulator columns are heads 2t and 2t+1: fetch their factors
     const float aa = __shfl_sync(kFull, alpha, 8 * t);
@@ -252,27 +269,38 @@ __device__ __forceinline__ void softmax_update(const float (&sc0)[4], const floa
     }
 }
 
+// Scores q.K of the 16 tokens of one bf16 tile: sc[0] tokens 0-7, sc[1]
+// tokens 8-15 (C fragments: row = head, column = token).
 template <int D>
-__device__ __forceinline__ void block_bf16(uint32_t kbase, uint32_t vbase, int nvalid,
-                                           const uint32_t (&qa0)[D / 16],
-                                           const uint32_t (&qa2)[D / 16], float sl2, float& m,
-                                           float& l, float (&o)[D / 16][4], int lane)
+__device__ __forceinline__ void scores_bf16(uint32_t kbase, const uint32_t (&qa0)[D / 16],
+                                            const uint32_t (&qa2)[D / 16], float (&sc)[2][4],
+                                            int lane)
+{
+    using G = Geom<D, false>;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int tok = ri + 8 * (mi >> 1);
+    const int csel = mi & 1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sc[0][k] = sc[1][k] = 0.f;
+#pragma unroll
+    for (int s = 0; s < G::KSTEPS; ++s) {
+        uint32_t r[4];
+        ldsm_x4(r, kbase + tile_off<G>(tok, 2 * s + csel));
+        mma_bf16(sc[0], qa0[s], 0u, qa2[s], 0u, r[0], r[1]);
+        mma_bf16(sc[1], qa0[s], 0u, qa2[s], 0u, r[2], r[3]);
+    }
+}
+
+// O^T += V^T P^T for one bf16 tile; P is split into bf16 hi + lo parts.
+template <int D>
+__device__ __forceinline__ void pv_bf16(uint32_t vbase, int nvalid, const float (&pr)[4],
+                                        float (&o)[D / 16][4], int lane)
 {
     using G = Geom<D, false>;
     const int t = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;
     const int tok = ri + 8 * (mi >> 1);
     const int csel = mi & 1;
-    float sc0[4] = {0.f, 0.f, 0.f, 0.f}, sc1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int s = 0; s < G::KSTEPS; ++s) {
-        uint32_t r[4];
-        ldsm_x4(r, kbase + tile_off<G>(tok, 2 * s + csel));
-        mma_bf16(sc0, qa0[s], 0u, qa2[s], 0u, r[0], r[1]);
-        mma_bf16(sc1, qa0[s], 0u, qa2[s], 0u, r[2], r[3]);
-    }
-    float pr[4];
-    softmax_update<D>(sc0, sc1, nvalid, sl2, m, l, o, pr, lane);
     const uint32_t h0 = pack_bf16x2(pr[0], pr[1]);
     const uint32_t h1 = pack_bf16x2(pr[2], pr[3]);
     const uint32_t e0 = pack_bf16x2(pr[0] - bf16_lo(h0), pr[1] - bf16_hi(h0));
@@ -293,18 +321,18 @@ __device__ __forceinline__ void block_bf16(uint32_t kbase, uint32_t vbase, int n
     }
 }
 
+// Scores of one E4M3 tile: bytes via ldmatrix, widened to f16 in registers.
 template <int D>
-__device__ __forceinline__ void block_fp8(uint32_t kbase, uint32_t vbase, int nvalid,
-                                          const uint32_t (&qa0)[D / 16],
-                                          const uint32_t (&qa2)[D / 16], float sl2, float& m,
-                                          float& l, float (&o)[D / 16][4], int lane)
+__device__ __forceinline__ void scores_fp8(uint32_t kbase, const uint32_t (&qa0)[D / 16],
+                                           const uint32_t (&qa2)[D / 16], float (&sc)[2][4],
+                                           int lane)
 {
     using G = Geom<D, true>;
-    const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;
     const int tok = ri + 8 * (mi & 1);
     const int csel = mi >> 1;
-    float sc0[4] = {0.f, 0.f, 0.f, 0.f}, sc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sc[0][k] = sc[1][k] = 0.f;
 #pragma unroll
     for (int c = 0; c < G::KSTEPS; c += 2) {
         uint32_t r[4];
@@ -312,13 +340,20 @@ __device__ __forceinline__ void block_fp8(uint32_t kbase, uint32_t vbase, int nv
         uint32_t b[4][2];
 #pragma unroll
         for (int j = 0; j < 4; ++j) e4m3x4_to_f16x2x2(r[j], b[j][0], b[j][1]);
-        mma_f16(sc0, qa0[c], 0u, qa2[c], 0u, b[0][0], b[0][1]);
-        mma_f16(sc1, qa0[c], 0u, qa2[c], 0u, b[1][0], b[1][1]);
-        mma_f16(sc0, qa0[c + 1], 0u, qa2[c + 1], 0u, b[2][0], b[2][1]);
-        mma_f16(sc1, qa0[c + 1], 0u, qa2[c + 1], 0u, b[3][0], b[3][1]);
+        mma_f16(sc[0], qa0[c], 0u, qa2[c], 0u, b[0][0], b[0][1]);
+        mma_f16(sc[1], qa0[c], 0u, qa2[c], 0u, b[1][0], b[1][1]);
+        mma_f16(sc[0], qa0[c + 1], 0u, qa2[c + 1], 0u, b[2][0], b[2][1]);
+        mma_f16(sc[1], qa0[c + 1], 0u, qa2[c + 1], 0u, b[3][0], b[3][1]);
     }
-    float pr[4];
-    softmax_update<D>(sc0, sc1, nvalid, sl2, m, l, o, pr, lane);
+}
+
+// O^T += V^T P^T for one E4M3 tile; P in f16.
+template <int D>
+__device__ __forceinline__ void pv_fp8(uint32_t vbase, int nvalid, const float (&pr)[4],
+                                       float (&o)[D / 16][4], int lane)
+{
+    using G = Geom<D, true>;
+    const int g = lane >> 2, t = lane & 3;
     const uint32_t pf0 = pack_f16x2(pr[0], pr[1]);
     const uint32_t pf1 = pack_f16x2(pr[2], pr[3]);
     // V rows of tokens 2t, 2t+1, 2t+8, 2t+9, bytes [BYTES*g, BYTES*g + BYTES)
@@ -356,6 +391,31 @@ __device__ __forceinline__ void block_fp8(uint32_t kbase, uint32_t vbase, int nv
             e4m3x4_to_f16x2x2(__byte_perm(x[2][w], x[3][w], sel), a[2], a[3]);
             mma_f16(o[2 * w + e], a[0], a[1], a[2], a[3], pf0, pf1);
         }
+    }
+}
+
+// NBK consecutive tiles of one pair (K at kb[j], V right after it): scores
+// of every tile first, one softmax update over all of them, then P.V.
+template <int D, bool FP8, int NBK>
+__device__ __forceinline__ void attend_tiles(const uint32_t (&kb)[NBK], int nvalid_last,
+                                             const uint32_t (&qa0)[D / 16],
+                                             const uint32_t (&qa2)[D / 16], float sl2, float& m,
+                                             float& l, float (&o)[D / 16][4], int lane)
+{
+    using G = Geom<D, FP8>;
+    float sc[NBK][2][4];
+#pragma unroll
+    for (int j = 0; j < NBK; ++j) {
+        if (FP8) scores_fp8<D>(kb[j], qa0, qa2, sc[j], lane);
+        else scores_bf16<D>(kb[j], qa0, qa2, sc[j], lane);
+    }
+    float pr[NBK][4];
+    softmax_update<D, NBK>(sc, nvalid_last, sl2, m, l, o, pr, lane);
+#pragma unroll
+    for (int j = 0; j < NBK; ++j) {
+        const int nv = j == NBK - 1 ? nvalid_last : kBlock;
+        if (FP8) pv_fp8<D>(kb[j] + G::TILE, nv, pr[j], o, lane);
+        else pv_bf16<D>(kb[j] + G::TILE, nv, pr[j], o, lane);
     }
 }
 
@@ -672,6 +732,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int j = 0; j < npro; ++j) issue(j, j);
 
     // ---- 4. main loop ------------------------------------------------------------
+    // Two consecutive tiles of the same pair are consumed together where the
+    // range allows: one softmax update and one loop turn per 32 tokens.
     uint32_t qa0[D / 16], qa2[D / 16];
     float o[D / 16][4];
     float m = -INFINITY, l = 0.f;
@@ -679,23 +741,26 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     int seg_pair = -1;
     int st = 0;
     uint32_t phase = 0;
-    for (int i = 0; i < cnt; ++i) {
-        bool ok = mbar_wait_bounded(bar0 + st * 8, phase, kWaitLimit);
+    // Wait for unit i in stage `sst`; on time-out flag the error and let the
+    // copies of units [i, issued_end) land before the warp gives up.
+    auto wait_unit = [&](int i, int sst, uint32_t ph, int issued_end) -> bool {
+        bool ok = mbar_wait_bounded(bar0 + sst * 8, ph, kWaitLimit);
         ok = __all_sync(kFull, ok);
         if (!ok) {
             if (lane == 0) {
                 raise_flag(&g_decode_err, KV_DEVERR_PIPELINE_TIMEOUT, i);
-                // let the copies still in flight land before the CTA retires
-                int sst = st;
-                uint32_t ph = phase;
-                for (int k = 0; k < ST && i + k < cnt; ++k) {
+                for (int j = i; j < issued_end; ++j) {
                     mbar_wait_bounded(bar0 + sst * 8, ph, kWaitLimit);
                     if (++sst == ST) { sst = 0; ph ^= 1u; }
                 }
             }
             __syncwarp();
-            return;
         }
+        return ok;
+    };
+    for (int i = 0; i < cnt;) {
+        const int issued_end = min(cnt, i + ST);
+        if (!wait_unit(i, st, phase, issued_end)) return;
         const int4 mt = meta[st];
         const bool valid = mt.x >= 0;
         const int pair = valid ? mt.x : -1 - mt.x;
@@ -713,18 +778,46 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
             for (int a = 0; a < D / 16; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
         }
-        seg_last = blk;
-        if (valid) {
-            const int nvalid = min(kBlock, L - blk * kBlock);
-            const uint32_t kb = stage0 + (uint32_t)(st * G::STAGE);
-            if (p.k_new != nullptr && nvalid == L - blk * kBlock)     // the pair's last block
-                append_patch<D, FP8>(p, seg_s, seg_h, mt.w, L, kb, kb + G::TILE, lane);
-            if (FP8) block_fp8<D>(kb, kb + G::TILE, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
-            else block_bf16<D>(kb, kb + G::TILE, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
+        const int st2 = st + 1 == ST ? 0 : st + 1;
+        const uint32_t phase2 = st + 1 == ST ? phase ^ 1u : phase;
+        bool two = false;
+        if (valid && i + 1 < cnt) {
+            __syncwarp();            // unit i+1's metadata was written by lane 0
+            two = meta[st2].x == mt.x;
         }
-        __syncwarp();
-        if (i + ST < cnt) issue(i + ST, st);
-        if (++st == ST) { st = 0; phase ^= 1u; }
+        const uint32_t kb = stage0 + (uint32_t)(st * G::STAGE);
+        if (two) {
+            if (!wait_unit(i + 1, st2, phase2, issued_end)) return;
+            const int id2 = meta[st2].w;
+            const uint32_t kb2 = stage0 + (uint32_t)(st2 * G::STAGE);
+            const int rest = L - (blk + 1) * kBlock;
+            const int nvalid = min(kBlock, rest);
+            if (p.k_new != nullptr && nvalid == rest)     // the pair's last block
+                append_patch<D, FP8>(p, seg_s, seg_h, id2, L, kb2, kb2 + G::TILE, lane);
+            const uint32_t kbs[2] = {kb, kb2};
+            attend_tiles<D, FP8, 2>(kbs, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
+            seg_last = blk + 1;
+            __syncwarp();
+            if (i + ST < cnt) issue(i + ST, st);
+            if (i + 1 + ST < cnt) issue(i + 1 + ST, st2);
+            st = st2 + 1 == ST ? 0 : st2 + 1;
+            phase = st2 + 1 == ST ? phase2 ^ 1u : phase2;
+            i += 2;
+        } else {
+            seg_last = blk;
+            if (valid) {
+                const int nvalid = min(kBlock, L - blk * kBlock);
+                if (p.k_new != nullptr && nvalid == L - blk * kBlock)     // the pair's last block
+                    append_patch<D, FP8>(p, seg_s, seg_h, mt.w, L, kb, kb + G::TILE, lane);
+                const uint32_t kbs[1] = {kb};
+                attend_tiles<D, FP8, 1>(kbs, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
+            }
+            __syncwarp();
+            if (i + ST < cnt) issue(i + ST, st);
+            st = st2;
+            phase = phase2;
+            i += 1;
+        }
     }
     if (seg_s >= 0)
         finalize<D, FP8>(p, w, q, seg_s, seg_h, seg_first, seg_last, seg_L, b0 + seg_i0, m, l, o,
