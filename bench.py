@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "375a4c1dd6128210d7ceb15c99105e866319bc0aaa2ef502b1f86c1c6d9f94c3",
-           "bytes_per_launch": 1089233920,
+TRAFFIC = {"kernel_sha256": "ad61123d1eca57e89a5eac38fb2cf0b37f0c0a87c338c7b63b325a82ebf347bc",
+           "bytes_per_launch": 1088652288,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,179,392 B + 3,129,088 B), scaled x4 by units processed "
+                     "(269,144,576 B + 3,018,496 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 
@@ -57,6 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (profiling a smaller case)")
+    ap.add_argument("--prefix", action="store_true",
+                    help="also time the shared-prefix step (paged_decode_prefix with the "
+                         "chunks kv_prefix_chunks finds) beside the plain one")
     return ap.parse_args(argv)
 
 
@@ -396,6 +399,37 @@ def run_ours(args):
     split_ms = statistics.mean(sp_ev[i][0].elapsed_time(sp_ev[i][1]) for i in range(K))
     merge_ms = statistics.mean(sp_ev[i][1].elapsed_time(sp_ev[i][2]) for i in range(K))
 
+    # shared-prefix step: the chunk table is built once on the host from the
+    # block tables (kv_prefix_chunks), the step reads each shared tile once
+    # per chunk of sequences
+    prefix = None
+    if args.prefix:
+        chunks_np, seq_chunk_np = pk.prefix_chunks(case.block_tables, case.context_lens,
+                                                   Hq // Hkv)
+        nc = len(chunks_np)
+        dch = torch.from_numpy(chunks_np).to(device)
+        dsc = torch.from_numpy(seq_chunk_np).to(device)
+        wsp = pk.alloc_prefix_workspace(B, nc, Hq, Hkv, D, case.kv_dtype, device=device)
+
+        def step_prefix():
+            pk.paged_decode_prefix(out, q, kc, vc, bt, cl, dch, dsc, case.scale, wsp,
+                                   case.k_scale, case.v_scale, k_new=k_new, v_new=v_new,
+                                   stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step_prefix()
+        pms_local, _ = timed(K, lambda e: step_prefix(), 0)
+        pms = reduce_max(pms_local, world, device)
+        flags, detail = pk.get_device_error()
+        assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
+        read_bytes = kv_bytes - sum(int(r[0]) * (int(r[1]) - 1) for r in chunks_np) * \
+            Hkv * 2 * 16 * D * case.elem_bytes
+        prefix = {"us_per_step": pms * 1e3, "chunks": nc,
+                  "kv_gbs_logical": kv_bytes / (pms * 1e-3) / 1e9,
+                  "kv_bytes_read": read_bytes,
+                  "kv_gbs_read": read_bytes / (pms * 1e-3) / 1e9,
+                  "plain_us_per_step": ms * 1e3, "speedup_vs_plain": ms / pms}
+
     # one fused step captured in a CUDA graph and replayed, each replay
     # bracketed by events: the median is the per-layer-step latency
     gs = torch.cuda.Stream(device)
@@ -515,6 +549,8 @@ def run_ours(args):
                            parallelism="replicas x%d" % world if world > 1 else "single GPU"),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
             "unfused": unfused, "graph_replay": graph_replay}
+    if prefix is not None:
+        line["prefix"] = prefix
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     if rank == 0:

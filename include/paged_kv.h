@@ -65,6 +65,7 @@ extern "C" {
 #define KV_DEVERR_BLOCK_OUT_OF_RANGE 2    /* a block-table entry outside [0, num_blocks) */
 #define KV_DEVERR_CONTEXT_TOO_LONG 4      /* context_lens[s] > 16*max_blocks_per_seq, or < 0 */
 #define KV_DEVERR_PIPELINE_TIMEOUT 8      /* a bulk copy never arrived (a bug, never expected) */
+#define KV_DEVERR_BAD_PREFIX 16           /* a prefix chunk table entry is inconsistent */
 
 /* ------------------------------------------------------------------ sizing */
 
@@ -312,6 +313,73 @@ int paged_decode_attention_noalloc(void* out, int out_dtype, const void* q, cons
                                    int max_blocks_per_seq, const int32_t* context_lens,
                                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                    float scale, void* stream);
+
+/* --------------------------------------------------- shared-prefix decoding */
+
+/* Requests that share a system prompt share its KV blocks ("KV cache complete
+ * guide", sections "(3) Prefix Caching" and "(4) PagedAttention": the same
+ * physical blocks, copy-on-write).  The entry points below read each shared
+ * (block, KV head) tile once for a whole chunk of sequences instead of once
+ * per sequence.  (An interface of this implementation; the pages describe
+ * the sharing, not a kernel for it.)
+ *
+ * A prefix chunk is a set of 2..KV_PREFIX_MAX_ROWS/G sequences (G = query
+ * heads per KV head) whose block-table rows start with the same P block ids,
+ * all P blocks lying wholly before each member's new token (16*P <=
+ * context_lens[s] - 1).  Chunk table: int32 [num_chunks][KV_PREFIX_CHUNK_INTS],
+ * row c = {P, m, member_0, ..., member_{m-1}, -1 ...}; the shared blocks are
+ * read from member_0's block-table row.  seq_chunk: int32 [num_seqs],
+ * (c << 4) | (index of s among chunk c's members), or -1 for a sequence in no
+ * chunk.  Each chunk's query rows (m * G <= 16) are attended together over
+ * its P blocks; every sequence then attends alone from block P (0 without a
+ * chunk) on, and the two partial results are combined by their log-sum-exp
+ * weights.  The result equals paged_decode_attention / paged_decode_step on
+ * the same inputs up to floating-point summation order. */
+#define KV_PREFIX_MAX_ROWS 16
+#define KV_PREFIX_MAX_MEMBERS 16
+#define KV_PREFIX_CHUNK_INTS (2 + KV_PREFIX_MAX_MEMBERS)
+
+/* Build a chunk table from block tables (host memory, plain C):
+ *   - sequences whose rows begin with the same block id and have at least
+ *     min_blocks full blocks before their new token form a group;
+ *   - each member's shared run is the number of leading block ids it has in
+ *     common with the group's leader -- its member with the most full blocks
+ *     before the new token, the first such -- capped by both members' full
+ *     blocks before their new tokens;
+ *   - members are ordered by shared run (longest first, then by index) and
+ *     cut into chunks of up to KV_PREFIX_MAX_ROWS / group_size sequences;
+ *     a chunk's P is its shortest member run; chunks with fewer than two
+ *     members or P < min_blocks are dropped (their sequences get -1).
+ * chunks must hold num_seqs / 2 rows (the most chunks possible); seq_chunk
+ * num_seqs entries.  group_size = num_q_heads / num_kv_heads (1..8).
+ * Returns KV_OK and *num_chunks, or KV_ERR_INVALID_ARG. */
+int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int group_size, int min_blocks,
+                     int32_t* chunks, int32_t* seq_chunk, int* num_chunks);
+
+/* Workspace bytes paged_decode_prefix needs (as paged_decode_workspace_bytes,
+ * with num_chunks prefix chunks). */
+int paged_decode_prefix_workspace_bytes(int num_seqs, int num_chunks, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int kv_dtype,
+                                        size_t* bytes);
+
+/* Decode attention with shared prefixes: arguments as paged_decode_step,
+ * plus the device copies of a chunk table and seq_chunk (above) and
+ * num_chunks (0 gives plain decoding).  k_new and v_new may both be NULL:
+ * then nothing is appended (as paged_decode_attention) and k_cache /
+ * v_cache are only read.  A chunk entry that breaks the rules above (P out
+ * of range, a member index outside [0, num_seqs), a shared block reaching a
+ * member's new token, a seq_chunk entry naming another chunk) flags
+ * KV_DEVERR_BAD_PREFIX; every access stays in bounds, the results of the
+ * sequences concerned are undefined.  The chunk table must describe blocks
+ * that really are shared: the kernel reads them from member_0's row. */
+int paged_decode_prefix(void* out, int out_dtype, const void* q, const void* k_new,
+                        const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                        float k_scale, float v_scale, int num_blocks, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                        const int32_t* chunks, const int32_t* seq_chunk, int num_chunks,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------- diagnostics */
 

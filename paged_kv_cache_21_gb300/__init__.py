@@ -39,6 +39,7 @@ DEVERR_SLOT_OUT_OF_RANGE = 1
 DEVERR_BLOCK_OUT_OF_RANGE = 2
 DEVERR_CONTEXT_TOO_LONG = 4
 DEVERR_PIPELINE_TIMEOUT = 8
+DEVERR_BAD_PREFIX = 16
 
 _ERRNAMES = {KV_ERR_INVALID_ARG: "KV_ERR_INVALID_ARG", KV_ERR_OUT_OF_BLOCKS: "KV_ERR_OUT_OF_BLOCKS",
              KV_ERR_UNSUPPORTED: "KV_ERR_UNSUPPORTED", KV_ERR_CUDA: "KV_ERR_CUDA",
@@ -87,6 +88,11 @@ _SIGS = {
                                _i, _i, _f, _p, ctypes.c_size_t, _p]),
     "paged_decode_attention_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
                                             _i, _i, _i, _f, _p]),
+    "kv_prefix_chunks": (_i, [_p, _i, _p, _i, _i, _i, _p, _p, ctypes.POINTER(_i)]),
+    "paged_decode_prefix_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i,
+                                                 ctypes.POINTER(ctypes.c_size_t)]),
+    "paged_decode_prefix": (_i, [_p, _i, _p, _p, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i,
+                                 _i, _i, _f, _p, _p, _i, _p, ctypes.c_size_t, _p]),
     "kv_get_device_error": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_i64)]),
     "kv_version": (ctypes.c_char_p, []),
 }
@@ -320,6 +326,68 @@ def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, cont
         _dptr(block_tables), block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D,
         float(scale), _dptr(workspace), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream)), "paged_decode_step")
+
+
+PREFIX_CHUNK_INTS = 18      # KV_PREFIX_CHUNK_INTS
+PREFIX_MAX_ROWS = 16        # KV_PREFIX_MAX_ROWS
+
+
+def prefix_chunks(block_tables, context_lens, group_size, min_blocks=1):
+    """Prefix chunks of sequences whose block tables start with the same
+    blocks (host numpy int32 arrays in, kv_prefix_chunks): returns
+    (chunks int32 [nc, 18], seq_chunk int32 [B])."""
+    import numpy as np
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, mb = bt.shape
+    chunks = np.full((max(B // 2, 1), PREFIX_CHUNK_INTS), -1, dtype=np.int32)
+    seq_chunk = np.full(max(B, 1), -1, dtype=np.int32)
+    nc = ctypes.c_int(0)
+    _check(_lib.kv_prefix_chunks(_np_ptr(bt), mb, _np_ptr(cl), B, int(group_size),
+                                 int(min_blocks), _np_ptr(chunks), _np_ptr(seq_chunk),
+                                 ctypes.byref(nc)), "kv_prefix_chunks")
+    return chunks[:nc.value].copy(), seq_chunk[:B].copy()
+
+
+def prefix_workspace_bytes(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
+                           kv_dtype=BF16):
+    n = ctypes.c_size_t(0)
+    _check(_lib.paged_decode_prefix_workspace_bytes(num_seqs, num_chunks, num_q_heads,
+                                                    num_kv_heads, head_dim, kv_dtype,
+                                                    ctypes.byref(n)),
+           "paged_decode_prefix_workspace_bytes")
+    return n.value
+
+
+def alloc_prefix_workspace(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
+                           kv_dtype=BF16, device=None):
+    import torch
+    nbytes = prefix_workspace_bytes(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
+                                    kv_dtype)
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_decode_prefix(out, q, k_cache, v_cache, block_tables, context_lens, chunks, seq_chunk,
+                        scale, workspace, k_scale=1.0, v_scale=1.0, k_new=None, v_new=None,
+                        stream=None):
+    """Decode attention with shared prefixes read once per chunk: chunks
+    int32 [nc, 18] and seq_chunk int32 [B] on the device (from
+    prefix_chunks); with k_new/v_new the step's token is appended first (as
+    paged_decode_step).  Other arguments as paged_decode_attention."""
+    import torch
+    B, Hq, D = q.shape
+    NB, Hkv, _, _ = k_cache.shape
+    out_dtype = F32 if out.dtype == torch.float32 else BF16
+    nc = int(chunks.shape[0])
+    null = ctypes.c_void_p(0)
+    _check(_lib.paged_decode_prefix(
+        _dptr(out), out_dtype, _dptr(q), _dptr(k_new) if k_new is not None else null,
+        _dptr(v_new) if v_new is not None else null, _dptr(k_cache), _dptr(v_cache),
+        _cache_dtype(k_cache), float(k_scale), float(v_scale), NB, _dptr(block_tables),
+        block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D, float(scale),
+        _dptr(chunks) if nc else null, _dptr(seq_chunk) if nc else null, nc, _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+        "paged_decode_prefix")
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -9,8 +9,10 @@
 // copy-on-write); "Transformer attention mask and KV cache inference",
 // section "Position ID and append contract" (a cache handle owns its length;
 // the new token goes at position == current length).
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
@@ -270,6 +272,85 @@ int kv_slot_mapping(const int32_t* block_tables, int max_blocks, const int64_t* 
         if (blk < 0) return KV_ERR_INVALID_ARG;
         slot_mapping[i] = (int64_t)blk * KV_BLOCK_SIZE + pos % KV_BLOCK_SIZE;
     }
+    return KV_OK;
+}
+
+// Prefix chunks from block tables ("KV cache complete guide", sections "(3)
+// Prefix Caching" and "(4) PagedAttention": requests with a common system
+// prompt hold the same physical blocks).  Groups by first block id, measures
+// each member's common run with the group's longest member, orders members
+// by that run and cuts them into chunks whose query rows fit one 16-row tile.
+int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int group_size, int min_blocks,
+                     int32_t* chunks, int32_t* seq_chunk, int* num_chunks)
+{
+    if (!num_chunks || num_seqs < 0 || max_blocks_per_seq <= 0 || group_size < 1 ||
+        group_size > 8 || min_blocks < 1)
+        return KV_ERR_INVALID_ARG;
+    *num_chunks = 0;
+    if (num_seqs == 0) return KV_OK;
+    if (!block_tables || !context_lens || !chunks || !seq_chunk) return KV_ERR_INVALID_ARG;
+    const int per_chunk = std::min(KV_PREFIX_MAX_ROWS / group_size, KV_PREFIX_MAX_MEMBERS);
+    const int32_t* bt = block_tables;
+    // full blocks before each sequence's new token (position L-1)
+    std::vector<int> usable(num_seqs, 0);
+    for (int s = 0; s < num_seqs; ++s) {
+        seq_chunk[s] = -1;
+        const int L = context_lens[s];
+        if (L < 1) continue;
+        usable[s] = std::min((L - 1) / KV_BLOCK_SIZE, max_blocks_per_seq);
+    }
+    // groups keyed by first block id, in order of first appearance
+    std::map<int32_t, int> key_to_group;
+    std::vector<std::vector<int>> groups;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (usable[s] < min_blocks) continue;
+        const int32_t first = bt[(int64_t)s * max_blocks_per_seq];
+        if (first < 0) continue;
+        auto it = key_to_group.find(first);
+        if (it == key_to_group.end()) {
+            key_to_group.emplace(first, (int)groups.size());
+            groups.push_back({s});
+        } else {
+            groups[it->second].push_back(s);
+        }
+    }
+    int nc = 0;
+    for (const auto& gm : groups) {
+        if (gm.size() < 2) continue;
+        // the member with the most full blocks before its new token (the
+        // first such) leads: every other member's run is measured on its row
+        int lead = gm[0];
+        for (int s : gm)
+            if (usable[s] > usable[lead]) lead = s;
+        const int32_t* lrow = bt + (int64_t)lead * max_blocks_per_seq;
+        std::vector<std::pair<int, int>> run;    // (shared run, sequence)
+        for (int s : gm) {
+            const int32_t* row = bt + (int64_t)s * max_blocks_per_seq;
+            const int cap = std::min(usable[s], usable[lead]);
+            int r = 0;
+            while (r < cap && row[r] == lrow[r] && row[r] >= 0) ++r;
+            run.emplace_back(r, s);
+        }
+        std::stable_sort(run.begin(), run.end(), [](const std::pair<int, int>& a,
+                                                    const std::pair<int, int>& b) {
+            return a.first > b.first;
+        });
+        for (size_t i0 = 0; i0 < run.size(); i0 += per_chunk) {
+            const size_t i1 = std::min(run.size(), i0 + (size_t)per_chunk);
+            const int m = (int)(i1 - i0);
+            const int P = run[i1 - 1].first;
+            if (m < 2 || P < min_blocks) continue;
+            int32_t* row = chunks + (int64_t)nc * KV_PREFIX_CHUNK_INTS;
+            row[0] = P;
+            row[1] = m;
+            for (int k = 0; k < KV_PREFIX_MAX_MEMBERS; ++k)
+                row[2 + k] = k < m ? run[i0 + k].second : -1;
+            for (int k = 0; k < m; ++k) seq_chunk[run[i0 + k].second] = (nc << 4) | k;
+            ++nc;
+        }
+    }
+    *num_chunks = nc;
     return KV_OK;
 }
 

@@ -67,6 +67,7 @@ constexpr int kWarpStageBytesFp8 = 24576;
 constexpr int kMinCtasBf16 = 1;
 constexpr int kMinCtasFp8 = 1;
 constexpr int kMinBlocksPerWarp = 16;            // do not split below 256 tokens per warp
+constexpr int kMinBlocksPerWarpChunk = 4;        // the same for the prefix chunk phase
 constexpr long long kWaitLimit = 1LL << 31;      // ~1 s of SM clocks
 
 template <int D, bool FP8>
@@ -111,9 +112,10 @@ struct DecodeParams {
     void* out;               // [B][Hq][D] bf16 or f32
     const int32_t* bt;       // [B][max_blocks]
     const int32_t* ctx;      // [B]
-    float* part_o;           // [slots][G][D]
-    float2* part_ml;         // [slots][G]  (max in log2 units, sum)
-    int2* pair_meta;         // [B*Hkv]  (first warp, number of partials)
+    float* part_o;           // [slots][prow][D]
+    float2* part_ml;         // [slots][prow]  (max in log2 units, sum)
+    int4* pair_meta;         // [streams*Hkv]  (first warp, number of partials,
+                             //  the sequence's (chunk << 4 | member) or -1, 0)
     const uint16_t* k_new;   // bf16 [B][Hkv][D], or null: no append
     const uint16_t* v_new;
     uint8_t* k_cache;        // caches, written only by the fused append
@@ -124,6 +126,11 @@ struct DecodeParams {
     float v_scale;
     float k_qscale, v_qscale;    // quantisation scales of the fused append (E4M3)
     int out_f32;
+    const int32_t* chunk;        // prefix chunks [nc][KV_PREFIX_CHUNK_INTS]
+    const int32_t* seq_chunk;    // [B]: (chunk << 4) | member index, or -1
+    int nc;                      // number of prefix chunks
+    int prow;                    // rows per partial slot
+    int slot_base;               // first partial slot of the sequence phase
 };
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane)
@@ -144,47 +151,141 @@ __device__ __forceinline__ int warp_sum(int v)
 }
 
 // Context length of sequence s clamped to its block-table row; returns the
-// number of blocks.
-__device__ __forceinline__ int seq_blocks(const int32_t* ctx, int s, int max_blocks, int& Lc)
+// number of blocks.  The split kernel's helpers only read (no flag atomics,
+// so the compiler can batch their loads); the merge kernel, which visits
+// every sequence, reports bad entries (report = true).
+__device__ __forceinline__ int seq_blocks(const int32_t* ctx, int s, int max_blocks, int& Lc,
+                                          bool report = false)
 {
     int L = __ldg(ctx + s);
     const int cap = max_blocks * kBlock;
     if (L < 0 || L > cap) {
-        raise_flag(&g_decode_err, KV_DEVERR_CONTEXT_TOO_LONG, L);
+        if (report) raise_flag(&g_decode_err, KV_DEVERR_CONTEXT_TOO_LONG, L);
         L = L < 0 ? 0 : cap;
     }
     Lc = L;
     return (L + kBlock - 1) / kBlock;
 }
 
+// ------------------------------------------------------------------ streams
+//
+// The work is a list of streams, each a run of blocks of one block-table row
+// attended by a set of query rows, for every KV head.  Streams [0, nc) are
+// the prefix chunks -- the P leading blocks that a chunk of sequences share,
+// attended once for all the chunk's query rows (up to 16: NR == 2 kernels
+// process these) -- and stream nc + s is sequence s from its first block
+// past its chunk's P (from block 0 without shared prefixes; NR == 1 kernels).
+
+struct Stream {
+    int nblk;    // blocks (per KV head)
+    int base;    // first block: index into the block-table row
+    int row;     // sequence whose block-table row holds the blocks
+    int L;       // tokens of that row that count (masking of the last block)
+    int cj;      // sequence stream with a shared prefix: (chunk << 4) | member, else -1
+};
+
+// P of chunk c if its table row is usable (P in [0, max_blocks], 1..16
+// members, at most 16 query rows, member 0 a valid sequence), else -1.
+__device__ __forceinline__ int chunk_blocks(const int32_t* chunk, int c, int B, int G,
+                                            int max_blocks, int& lead, int& members,
+                                            bool report = false)
+{
+    const int32_t* row = chunk + (size_t)c * KV_PREFIX_CHUNK_INTS;
+    const int P = __ldg(row);
+    members = __ldg(row + 1);
+    lead = __ldg(row + 2);
+    if (P < 0 || P > max_blocks || members < 1 || members > KV_PREFIX_MAX_MEMBERS ||
+        members * G > KV_PREFIX_MAX_ROWS || lead < 0 || lead >= B) {
+        if (report) raise_flag(&g_decode_err, KV_DEVERR_BAD_PREFIX, c);
+        return -1;
+    }
+    return P;
+}
+
+// Shared leading blocks of sequence s (context L): its chunk's P when the
+// chunk is usable, s really is its member j, and the P blocks lie before the
+// new token; otherwise 0 (s is then attended alone, from block 0).
+__device__ __forceinline__ int prefix_of(const int32_t* chunk, const int32_t* seq_chunk, int nc,
+                                         int B, int G, int max_blocks, int s, int L, int& c,
+                                         int& j, bool report = false)
+{
+    const int sc = __ldg(seq_chunk + s);
+    if (sc < 0) return 0;
+    c = sc >> 4;
+    j = sc & 15;
+    int lead, members;
+    const int P = c < nc ? chunk_blocks(chunk, c, B, G, max_blocks, lead, members) : -1;
+    bool ok = P >= 0 && j < members &&
+              __ldg(chunk + (size_t)c * KV_PREFIX_CHUNK_INTS + 2 + j) == s;
+    if (ok && P > 0 && (L < 1 || P > (L - 1) / kBlock)) ok = false;
+    if (!ok) {
+        if (report) raise_flag(&g_decode_err, KV_DEVERR_BAD_PREFIX, s);
+        return 0;
+    }
+    return P;
+}
+
+template <int NR>
+__device__ __forceinline__ Stream stream_at(const DecodeParams& p, int sigma)
+{
+    Stream r;
+    if (NR == 2 && sigma < p.nc) {
+        int lead, members;
+        const int P = chunk_blocks(p.chunk, sigma, p.B, p.G, p.max_blocks, lead, members);
+        r.nblk = P > 0 ? P : 0;
+        r.base = 0;
+        r.row = P > 0 ? lead : 0;
+        r.L = r.nblk * kBlock;
+        r.cj = -1;
+        return r;
+    }
+    // (NR == 1 kernels run without prefix chunks: nc is 0 there)
+    if constexpr (NR == 2) sigma -= p.nc;
+    int L;
+    const int nb = seq_blocks(p.ctx, sigma, p.max_blocks, L);
+    r.row = sigma;
+    r.L = L;
+    r.base = 0;
+    r.cj = -1;
+    if (NR == 2 && p.nc > 0) {
+        int c = 0, j = 0;
+        r.base = prefix_of(p.chunk, p.seq_chunk, p.nc, p.B, p.G, p.max_blocks, sigma, L, c, j);
+        if (r.base > 0) r.cj = (c << 4) | j;
+    }
+    r.nblk = nb - r.base;
+    return r;
+}
+
 // One lane's entry of the block-id window.
 struct Win {
-    int id, s, h, blk, L;
+    int id, s, h, blk, L;    // s: the stream; blk: index into its block-table row
+    int base, row;           // the stream's first block and block-table row
 };
 
 // Fill the window for flat positions pos0 + lane (relative to the warp's
-// range start), walking forward from cursor (s, h, blk) where blk may equal
-// the pair's block count (then the walk moves on to the next pair).
-__device__ __forceinline__ void fill_window(Win& e, const DecodeParams& p, int s, int h, int blk,
-                                            int nb, int L, int pos0, int cnt, int lane)
+// range start), walking forward from stream sg, head h, block j of the
+// stream (j may equal the stream's block count: the walk then moves on).
+template <int NR>
+__device__ __forceinline__ void fill_window(Win& e, const DecodeParams& p, int ns, int sg, int h,
+                                            int j, Stream S, int pos0, int cnt, int lane)
 {
-    e.id = -1; e.s = 0; e.h = 0; e.blk = 0; e.L = 0;
+    e.id = -1; e.s = 0; e.h = 0; e.blk = 0; e.L = 0; e.base = 0; e.row = 0;
     if (pos0 + lane >= cnt) return;
     int r = lane;
-    while (r >= nb - blk) {
-        r -= nb - blk;
-        blk = 0;
+    while (r >= S.nblk - j) {
+        r -= S.nblk - j;
+        j = 0;
         if (++h == p.Hkv) {
             h = 0;
             do {
-                if (++s >= p.B) return;      // inconsistent input: leave the entry invalid
-                nb = seq_blocks(p.ctx, s, p.max_blocks, L);
-            } while (nb == 0);
+                if (++sg >= ns) return;      // inconsistent input: leave the entry invalid
+                S = stream_at<NR>(p, sg);
+            } while (S.nblk <= 0);
         }
     }
-    blk += r;
-    e.id = __ldg(p.bt + (size_t)s * p.max_blocks + blk);
-    e.s = s; e.h = h; e.blk = blk; e.L = L;
+    j += r;
+    e.id = __ldg(p.bt + (size_t)S.row * p.max_blocks + S.base + j);
+    e.s = sg; e.h = h; e.blk = S.base + j; e.L = S.L; e.base = S.base; e.row = S.row;
 }
 
 // Four E4M3 codes (bytes 0..3 of w) -> two f16x2: lo = (byte0, byte1), hi =
@@ -209,71 +310,96 @@ __device__ __forceinline__ int out_dim(int i, int g, int half)
 }
 
 // ------------------------------------------------------------ per-block math
+//
+// A unit's query rows sit in the rows of the 16-row MMA A operand: rows 0-7
+// always, rows 8-15 as well when NR == 2 (a prefix chunk with more than 8
+// query rows).  Lane (g = lane/4, t = lane%4) holds, per 8-token half of a
+// block, the scores of rows g (and g + 8) at tokens 2t and 2t+1.
 
-// Online-softmax update over NBK consecutive blocks of one pair, from each
-// block's scores of this lane's head (lane / 4) at tokens (2t, 2t+1, 2t+8,
-// 2t+9); only the last block may be partial (nvalid_last tokens).  Returns
-// the probabilities of those tokens and rescales the accumulator.
-template <int D, int NBK>
+// Online-softmax update over NBK consecutive blocks of one stream for the NR
+// row tiles, from each block's scores (only the last block may be partial:
+// nvalid_last tokens).  Returns the probabilities of the lane's tokens (2t,
+// 2t+1, 2t+8, 2t+9) and rescales the accumulators.
+template <int D, int NBK, int NR>
 __device__ __forceinline__ void softmax_update(const float (&sc)[NBK][2][4], int nvalid_last,
-                                               float sl2, float& m, float& l,
-                                               float (&o)[D / 16][4], float (&pr)[NBK][4],
-                                               int lane)
+                                               float sl2, float (&m)[NR], float (&l)[NR],
+                                               float (&o)[NR][D / 16][4],
+                                               float (&pr)[NBK][NR][4], int lane)
 {
     const int t = lane & 3;
-    float x[NBK][4];
+    float x[NBK][NR][4];
 #pragma unroll
     for (int j = 0; j < NBK; ++j) {
-        x[j][0] = sc[j][0][0] * sl2;
-        x[j][1] = sc[j][0][1] * sl2;
-        x[j][2] = sc[j][1][0] * sl2;
-        x[j][3] = sc[j][1][1] * sl2;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            x[j][r][0] = sc[j][0][2 * r] * sl2;
+            x[j][r][1] = sc[j][0][2 * r + 1] * sl2;
+            x[j][r][2] = sc[j][1][2 * r] * sl2;
+            x[j][r][3] = sc[j][1][2 * r + 1] * sl2;
+        }
     }
     if (nvalid_last < kBlock) {
         const int t0 = 2 * t;
-        if (t0 >= nvalid_last) x[NBK - 1][0] = -INFINITY;
-        if (t0 + 1 >= nvalid_last) x[NBK - 1][1] = -INFINITY;
-        if (t0 + 8 >= nvalid_last) x[NBK - 1][2] = -INFINITY;
-        if (t0 + 9 >= nvalid_last) x[NBK - 1][3] = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            if (t0 >= nvalid_last) x[NBK - 1][r][0] = -INFINITY;
+            if (t0 + 1 >= nvalid_last) x[NBK - 1][r][1] = -INFINITY;
+            if (t0 + 8 >= nvalid_last) x[NBK - 1][r][2] = -INFINITY;
+            if (t0 + 9 >= nvalid_last) x[NBK - 1][r][3] = -INFINITY;
+        }
     }
-    float mx = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
+    float alpha[NR];
+    bool rescale = false;
 #pragma unroll
-    for (int j = 1; j < NBK; ++j)
-        mx = fmaxf(mx, fmaxf(fmaxf(x[j][0], x[j][1]), fmaxf(x[j][2], x[j][3])));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    const float m_new = fmaxf(m, mx);
-    const float alpha = exp2f(m - m_new);
-    float sum = 0.f;
+    for (int r = 0; r < NR; ++r) {
+        float mx = fmaxf(fmaxf(x[0][r][0], x[0][r][1]), fmaxf(x[0][r][2], x[0][r][3]));
 #pragma unroll
-    for (int j = 0; j < NBK; ++j) {
-        pr[j][0] = exp2f(x[j][0] - m_new);
-        pr[j][1] = exp2f(x[j][1] - m_new);
-        pr[j][2] = exp2f(x[j][2] - m_new);
-        pr[j][3] = exp2f(x[j][3] - m_new);
-        sum += (pr[j][0] + pr[j][1]) + (pr[j][2] + pr[j][3]);
+        for (int j = 1; j < NBK; ++j)
+            mx = fmaxf(mx, fmaxf(fmaxf(x[j][r][0], x[j][r][1]), fmaxf(x[j][r][2], x[j][r][3])));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        const float m_new = fmaxf(m[r], mx);
+        alpha[r] = exp2f(m[r] - m_new);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < NBK; ++j) {
+            pr[j][r][0] = exp2f(x[j][r][0] - m_new);
+            pr[j][r][1] = exp2f(x[j][r][1] - m_new);
+            pr[j][r][2] = exp2f(x[j][r][2] - m_new);
+            pr[j][r][3] = exp2f(x[j][r][3] - m_new);
+            sum += (pr[j][r][0] + pr[j][r][1]) + (pr[j][r][2] + pr[j][r][3]);
+        }
+        l[r] = l[r] * alpha[r] + sum;
+        m[r] = m_new;
+        rescale = rescale || alpha[r] != 1.f;
     }
-    l = l * alpha + sum;
-    m = m_new;
-    // accumulator columns are heads 2t and 2t+1: fetch their factors
-    const float aa = __shfl_sync(kFull, alpha, 8 * t);
-    const float ab = __shfl_sync(kFull, alpha, 8 * t + 4);
-    if (__any_sync(kFull, aa != 1.f || ab != 1.f)) {
+    // accumulator columns are rows 2t and 2t+1 (+ 8r): fetch their factors
+    if (__any_sync(kFull, rescale)) {
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-            o[i][0] *= aa;
-            o[i][1] *= ab;
-            o[i][2] *= aa;
-            o[i][3] *= ab;
+        for (int r = 0; r < NR; ++r) {
+            const float aa = __shfl_sync(kFull, alpha[r], 8 * t);
+            const float ab = __shfl_sync(kFull, alpha[r], 8 * t + 4);
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                o[r][i][0] *= aa;
+                o[r][i][1] *= ab;
+                o[r][i][2] *= aa;
+                o[r][i][3] *= ab;
+            }
         }
     }
 }
 
-// Scores q.K of the 16 tokens of one bf16 tile: sc[0] tokens 0-7, sc[1]
-// tokens 8-15 (C fragments: row = head, column = token).
+// Query fragments of a unit: a0/a2 rows 0-7, a1/a3 rows 8-15 (used when NR == 2).
 template <int D>
-__device__ __forceinline__ void scores_bf16(uint32_t kbase, const uint32_t (&qa0)[D / 16],
-                                            const uint32_t (&qa2)[D / 16], float (&sc)[2][4],
+struct QFrag {
+    uint32_t a0[D / 16], a1[D / 16], a2[D / 16], a3[D / 16];
+};
+
+// Scores q.K of the 16 tokens of one bf16 tile: sc[0] tokens 0-7, sc[1]
+// tokens 8-15 (C fragments: row = query row, column = token).
+template <int D, int NR>
+__device__ __forceinline__ void scores_bf16(uint32_t kbase, const QFrag<D>& qf, float (&sc)[2][4],
                                             int lane)
 {
     using G = Geom<D, false>;
@@ -286,25 +412,31 @@ __device__ __forceinline__ void scores_bf16(uint32_t kbase, const uint32_t (&qa0
     for (int s = 0; s < G::KSTEPS; ++s) {
         uint32_t r[4];
         ldsm_x4(r, kbase + tile_off<G>(tok, 2 * s + csel));
-        mma_bf16(sc[0], qa0[s], 0u, qa2[s], 0u, r[0], r[1]);
-        mma_bf16(sc[1], qa0[s], 0u, qa2[s], 0u, r[2], r[3]);
+        const uint32_t a1 = NR == 2 ? qf.a1[s] : 0u, a3 = NR == 2 ? qf.a3[s] : 0u;
+        mma_bf16(sc[0], qf.a0[s], a1, qf.a2[s], a3, r[0], r[1]);
+        mma_bf16(sc[1], qf.a0[s], a1, qf.a2[s], a3, r[2], r[3]);
     }
 }
 
-// O^T += V^T P^T for one bf16 tile; P is split into bf16 hi + lo parts.
-template <int D>
-__device__ __forceinline__ void pv_bf16(uint32_t vbase, int nvalid, const float (&pr)[4],
-                                        float (&o)[D / 16][4], int lane)
+// O^T += V^T P^T for one bf16 tile and NR row tiles; P is split into bf16
+// hi + lo parts.
+template <int D, int NR>
+__device__ __forceinline__ void pv_bf16(uint32_t vbase, int nvalid, const float (&pr)[NR][4],
+                                        float (&o)[NR][D / 16][4], int lane)
 {
     using G = Geom<D, false>;
     const int t = lane & 3;
     const int mi = lane >> 3, ri = lane & 7;
     const int tok = ri + 8 * (mi >> 1);
     const int csel = mi & 1;
-    const uint32_t h0 = pack_bf16x2(pr[0], pr[1]);
-    const uint32_t h1 = pack_bf16x2(pr[2], pr[3]);
-    const uint32_t e0 = pack_bf16x2(pr[0] - bf16_lo(h0), pr[1] - bf16_hi(h0));
-    const uint32_t e1 = pack_bf16x2(pr[2] - bf16_lo(h1), pr[3] - bf16_hi(h1));
+    uint32_t h0[NR], h1[NR], e0[NR], e1[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        h0[r] = pack_bf16x2(pr[r][0], pr[r][1]);
+        h1[r] = pack_bf16x2(pr[r][2], pr[r][3]);
+        e0[r] = pack_bf16x2(pr[r][0] - bf16_lo(h0[r]), pr[r][1] - bf16_hi(h0[r]));
+        e1[r] = pack_bf16x2(pr[r][2] - bf16_lo(h1[r]), pr[r][3] - bf16_hi(h1[r]));
+    }
     uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
     if (nvalid < kBlock) {      // zero V rows past the context (they may hold anything)
         const int t0 = 2 * t;
@@ -313,18 +445,20 @@ __device__ __forceinline__ void pv_bf16(uint32_t vbase, int nvalid, const float 
     }
 #pragma unroll
     for (int i = 0; i < G::MTILES; ++i) {
-        uint32_t r[4];
-        ldsm_x4_trans(r, vbase + tile_off<G>(tok, 2 * i + csel));
-        r[0] &= m01; r[1] &= m01; r[2] &= m23; r[3] &= m23;
-        mma_bf16(o[i], r[0], r[1], r[2], r[3], h0, h1);
-        mma_bf16(o[i], r[0], r[1], r[2], r[3], e0, e1);
+        uint32_t r4[4];
+        ldsm_x4_trans(r4, vbase + tile_off<G>(tok, 2 * i + csel));
+        r4[0] &= m01; r4[1] &= m01; r4[2] &= m23; r4[3] &= m23;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            mma_bf16(o[r][i], r4[0], r4[1], r4[2], r4[3], h0[r], h1[r]);
+            mma_bf16(o[r][i], r4[0], r4[1], r4[2], r4[3], e0[r], e1[r]);
+        }
     }
 }
 
 // Scores of one E4M3 tile: bytes via ldmatrix, widened to f16 in registers.
-template <int D>
-__device__ __forceinline__ void scores_fp8(uint32_t kbase, const uint32_t (&qa0)[D / 16],
-                                           const uint32_t (&qa2)[D / 16], float (&sc)[2][4],
+template <int D, int NR>
+__device__ __forceinline__ void scores_fp8(uint32_t kbase, const QFrag<D>& qf, float (&sc)[2][4],
                                            int lane)
 {
     using G = Geom<D, true>;
@@ -340,22 +474,29 @@ __device__ __forceinline__ void scores_fp8(uint32_t kbase, const uint32_t (&qa0)
         uint32_t b[4][2];
 #pragma unroll
         for (int j = 0; j < 4; ++j) e4m3x4_to_f16x2x2(r[j], b[j][0], b[j][1]);
-        mma_f16(sc[0], qa0[c], 0u, qa2[c], 0u, b[0][0], b[0][1]);
-        mma_f16(sc[1], qa0[c], 0u, qa2[c], 0u, b[1][0], b[1][1]);
-        mma_f16(sc[0], qa0[c + 1], 0u, qa2[c + 1], 0u, b[2][0], b[2][1]);
-        mma_f16(sc[1], qa0[c + 1], 0u, qa2[c + 1], 0u, b[3][0], b[3][1]);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int k = c + cc;
+            const uint32_t a1 = NR == 2 ? qf.a1[k] : 0u, a3 = NR == 2 ? qf.a3[k] : 0u;
+            mma_f16(sc[0], qf.a0[k], a1, qf.a2[k], a3, b[2 * cc][0], b[2 * cc][1]);
+            mma_f16(sc[1], qf.a0[k], a1, qf.a2[k], a3, b[2 * cc + 1][0], b[2 * cc + 1][1]);
+        }
     }
 }
 
-// O^T += V^T P^T for one E4M3 tile; P in f16.
-template <int D>
-__device__ __forceinline__ void pv_fp8(uint32_t vbase, int nvalid, const float (&pr)[4],
-                                       float (&o)[D / 16][4], int lane)
+// O^T += V^T P^T for one E4M3 tile and NR row tiles; P in f16.
+template <int D, int NR>
+__device__ __forceinline__ void pv_fp8(uint32_t vbase, int nvalid, const float (&pr)[NR][4],
+                                       float (&o)[NR][D / 16][4], int lane)
 {
     using G = Geom<D, true>;
     const int g = lane >> 2, t = lane & 3;
-    const uint32_t pf0 = pack_f16x2(pr[0], pr[1]);
-    const uint32_t pf1 = pack_f16x2(pr[2], pr[3]);
+    uint32_t pf0[NR], pf1[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        pf0[r] = pack_f16x2(pr[r][0], pr[r][1]);
+        pf1[r] = pack_f16x2(pr[r][2], pr[r][3]);
+    }
     // V rows of tokens 2t, 2t+1, 2t+8, 2t+9, bytes [BYTES*g, BYTES*g + BYTES)
     constexpr int BYTES = D / 8;
     constexpr int WORDS = BYTES / 4;
@@ -389,56 +530,103 @@ __device__ __forceinline__ void pv_fp8(uint32_t vbase, int nvalid, const float (
             uint32_t a[4];
             e4m3x4_to_f16x2x2(__byte_perm(x[0][w], x[1][w], sel), a[0], a[1]);
             e4m3x4_to_f16x2x2(__byte_perm(x[2][w], x[3][w], sel), a[2], a[3]);
-            mma_f16(o[2 * w + e], a[0], a[1], a[2], a[3], pf0, pf1);
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+                mma_f16(o[r][2 * w + e], a[0], a[1], a[2], a[3], pf0[r], pf1[r]);
         }
     }
 }
 
-// NBK consecutive tiles of one pair (K at kb[j], V right after it): scores
-// of every tile first, one softmax update over all of them, then P.V.
-template <int D, bool FP8, int NBK>
+// NBK consecutive tiles of one stream (K at kb[j], V right after it), NR row
+// tiles: scores of every tile first, one softmax update over all of them,
+// then P.V.
+template <int D, bool FP8, int NBK, int NR>
 __device__ __forceinline__ void attend_tiles(const uint32_t (&kb)[NBK], int nvalid_last,
-                                             const uint32_t (&qa0)[D / 16],
-                                             const uint32_t (&qa2)[D / 16], float sl2, float& m,
-                                             float& l, float (&o)[D / 16][4], int lane)
+                                             const QFrag<D>& qf, float sl2, float (&m)[NR],
+                                             float (&l)[NR], float (&o)[NR][D / 16][4], int lane)
 {
     using G = Geom<D, FP8>;
     float sc[NBK][2][4];
 #pragma unroll
     for (int j = 0; j < NBK; ++j) {
-        if (FP8) scores_fp8<D>(kb[j], qa0, qa2, sc[j], lane);
-        else scores_bf16<D>(kb[j], qa0, qa2, sc[j], lane);
+        if (FP8) scores_fp8<D, NR>(kb[j], qf, sc[j], lane);
+        else scores_bf16<D, NR>(kb[j], qf, sc[j], lane);
     }
-    float pr[NBK][4];
-    softmax_update<D, NBK>(sc, nvalid_last, sl2, m, l, o, pr, lane);
+    float pr[NBK][NR][4];
+    softmax_update<D, NBK, NR>(sc, nvalid_last, sl2, m, l, o, pr, lane);
 #pragma unroll
     for (int j = 0; j < NBK; ++j) {
         const int nv = j == NBK - 1 ? nvalid_last : kBlock;
-        if (FP8) pv_fp8<D>(kb[j] + G::TILE, nv, pr[j], o, lane);
-        else pv_bf16<D>(kb[j] + G::TILE, nv, pr[j], o, lane);
+        if (FP8) pv_fp8<D, NR>(kb[j] + G::TILE, nv, pr[j], o, lane);
+        else pv_bf16<D, NR>(kb[j] + G::TILE, nv, pr[j], o, lane);
     }
 }
 
-// Query fragments of head (h*G + g) of sequence s (rows g >= G are zero).
-template <int D, bool FP8>
-__device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, int lane,
-                                       uint32_t (&qa0)[D / 16], uint32_t (&qa2)[D / 16])
+// The same, for a kernel holding NRK >= 1 row tiles of state of which the
+// stream uses nr (1 or NRK).
+template <int D, bool FP8, int NBK, int NRK>
+__device__ __forceinline__ void attend(int nr, const uint32_t (&kb)[NBK], int nvalid_last,
+                                       const QFrag<D>& qf, float sl2, float (&m)[NRK],
+                                       float (&l)[NRK], float (&o)[NRK][D / 16][4], int lane)
 {
-    const int g = lane >> 2, t = lane & 3;
-    const bool live = g < p.G;
-    const uint16_t* qh = p.q + ((size_t)s * p.Hq + (size_t)h * p.G + (live ? g : 0)) * D;
+    if constexpr (NRK == 2) {
+        if (nr == 2) {
+            attend_tiles<D, FP8, NBK, 2>(kb, nvalid_last, qf, sl2, m, l, o, lane);
+            return;
+        }
+    }
+    attend_tiles<D, FP8, NBK, 1>(kb, nvalid_last, qf, sl2,
+                                 *reinterpret_cast<float(*)[1]>(&m[0]),
+                                 *reinterpret_cast<float(*)[1]>(&l[0]),
+                                 *reinterpret_cast<float(*)[1][D / 16][4]>(&o[0]), lane);
+}
+
+// Query fragment rows of one query head (head index within sequence s);
+// `live` false gives a zero row.  bf16 keys: a holds elements (16k + 2t,
+// 16k + 2t + 1), b elements (16k + 8 + 2t, ...); E4M3 keys (f16 operands):
+// the four consecutive elements 16k + 4t .. 16k + 4t + 3, in the order
+// the byte-wise key fragments use.
+template <int D, bool FP8>
+__device__ __forceinline__ void load_q_row(const DecodeParams& p, int s, int head, bool live,
+                                           int lane, uint32_t (&a)[D / 16], uint32_t (&b)[D / 16])
+{
+    const int t = lane & 3;
+    const uint16_t* qh = p.q + ((size_t)(live ? s : 0) * p.Hq + (live ? head : 0)) * D;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
         if (!FP8) {
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
-            qa0[k] = live ? __ldg(q32 + 8 * k + t) : 0u;
-            qa2[k] = live ? __ldg(q32 + 8 * k + 4 + t) : 0u;
+            a[k] = live ? __ldg(q32 + 8 * k + t) : 0u;
+            b[k] = live ? __ldg(q32 + 8 * k + 4 + t) : 0u;
         } else {
             uint2 v = make_uint2(0u, 0u);
             if (live) v = __ldg(reinterpret_cast<const uint2*>(qh + 16 * k + 4 * t));
-            qa0[k] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
-            qa2[k] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
+            a[k] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
+            b[k] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
         }
+    }
+}
+
+// Query fragments of a stream: the G heads of KV head h of sequence s, or
+// (prefix chunk c) row r = j*G + i is head h*G + i of the chunk's member j.
+template <int D, bool FP8, int NR>
+__device__ __forceinline__ void load_q(const DecodeParams& p, bool chunk, int sc, int h, int rows,
+                                       int lane, QFrag<D>& qf)
+{
+    const int g = lane >> 2;
+    if (!chunk) {
+        load_q_row<D, FP8>(p, sc, h * p.G + g, g < p.G, lane, qf.a0, qf.a2);
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const int row = g + 8 * r;
+        const int j = row / p.G, i = row - j * p.G;
+        int s = -1;
+        if (row < rows) s = __ldg(p.chunk + (size_t)sc * KV_PREFIX_CHUNK_INTS + 2 + j);
+        const bool live = s >= 0 && s < p.B;
+        if (r == 0) load_q_row<D, FP8>(p, s, h * p.G + i, live, lane, qf.a0, qf.a2);
+        else load_q_row<D, FP8>(p, s, h * p.G + i, live, lane, qf.a1, qf.a3);
     }
 }
 
@@ -465,41 +653,61 @@ __device__ __forceinline__ void store4(const P& p, size_t idx, float a, float b,
     }
 }
 
-// End of a segment (a run of blocks of one pair inside this warp's range):
-// write the final output if the warp saw the whole pair, otherwise store a
-// partial for the merge kernel.  The warp holding the pair's block 0 also
-// records which warps hold the rest.  Only plain stores: a pair switch in
-// mid-range does not stall the warp's pipeline.
-template <int D, bool FP8>
-__device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, int s, int h,
-                                         int first_blk, int last_blk, int L, int flat_first,
-                                         float m, float l, const float (&o)[D / 16][4], int lane)
+// The run of units of one (stream, KV head) inside a warp's range.
+struct Seg {
+    int pair;          // stream * Hkv + h
+    int s;             // own stream: the sequence; prefix chunk: the chunk
+    int h;
+    bool chunk;
+    int rows;          // query rows (G, or members * G)
+    int nr;            // row tiles in use (1 or 2)
+    int base, end;     // the stream's blocks [base, end) of its block-table row
+    int first, last;   // the blocks this warp saw
+    int i0;            // position of the first of them in the warp's range
+    int cj;            // sequence with a shared prefix: (chunk << 4) | member, else -1
+};
+
+// End of a segment: write the final output if the warp saw a whole
+// sequence stream with no shared prefix, otherwise store a partial (rows of
+// the segment, unnormalised, with their (max, sum)) for the merge kernel.
+// The warp holding the stream's first block also records which warps hold
+// the rest.  Only plain stores: a stream switch in mid-range does not stall
+// the warp's pipeline.
+template <int D, bool FP8, int NR>
+__device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, int b0,
+                                         int slot_base, const Seg& sg,
+                                         const float (&m)[NR], const float (&l)[NR],
+                                         const float (&o)[NR][D / 16][4], int lane)
 {
     const int g = lane >> 2, t = lane & 3;
-    float lt = l + __shfl_xor_sync(kFull, l, 1);
-    lt += __shfl_xor_sync(kFull, lt, 2);
-    const float la = __shfl_sync(kFull, lt, 8 * t), lb = __shfl_sync(kFull, lt, 8 * t + 4);
-    const float ma = __shfl_sync(kFull, m, 8 * t), mb = __shfl_sync(kFull, m, 8 * t + 4);
-    const int nb = (L + kBlock - 1) / kBlock;
-    const int pair = s * p.Hkv + h;
-    const int ha = 2 * t, hb = 2 * t + 1;
-    if (first_blk == 0 && last_blk == nb - 1) {
-        const float ia = la > 0.f ? p.v_scale / la : 0.f;
-        const float ib = lb > 0.f ? p.v_scale / lb : 0.f;
-        const size_t row = (size_t)s * p.Hq + (size_t)h * p.G;
+    float la[NR], lb[NR], ma[NR], mb[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        float lt = l[r] + __shfl_xor_sync(kFull, l[r], 1);
+        lt += __shfl_xor_sync(kFull, lt, 2);
+        la[r] = __shfl_sync(kFull, lt, 8 * t);
+        lb[r] = __shfl_sync(kFull, lt, 8 * t + 4);
+        ma[r] = __shfl_sync(kFull, m[r], 8 * t);
+        mb[r] = __shfl_sync(kFull, m[r], 8 * t + 4);
+    }
+    if (!sg.chunk && sg.base == 0 && sg.first == 0 && sg.last == sg.end - 1) {
+        const int ha = 2 * t, hb = 2 * t + 1;
+        const float ia = la[0] > 0.f ? p.v_scale / la[0] : 0.f;
+        const float ib = lb[0] > 0.f ? p.v_scale / lb[0] : 0.f;
+        const size_t row = (size_t)sg.s * p.Hq + (size_t)sg.h * p.G;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int d = out_dim<D, FP8>(i, g, half);
                 if (ha < p.G) {
-                    const float v = o[i][2 * half] * ia;
+                    const float v = o[0][i][2 * half] * ia;
                     const size_t idx = (row + ha) * D + d;
                     if (p.out_f32) reinterpret_cast<float*>(p.out)[idx] = v;
                     else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
                 }
                 if (hb < p.G) {
-                    const float v = o[i][2 * half + 1] * ib;
+                    const float v = o[0][i][2 * half + 1] * ib;
                     const size_t idx = (row + hb) * D + d;
                     if (p.out_f32) reinterpret_cast<float*>(p.out)[idx] = v;
                     else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
@@ -507,27 +715,34 @@ __device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, in
             }
         }
     } else {
-        const size_t slot = (size_t)pair + w;
-        float* po = p.part_o + slot * p.G * D;
+        const size_t slot = (size_t)slot_base + sg.pair + w;
+        float* po = p.part_o + slot * p.prow * D;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
+        for (int r = 0; r < NR; ++r) {
+            if (r >= sg.nr) break;
+            const int ha = 8 * r + 2 * t, hb = ha + 1;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int d = out_dim<D, FP8>(i, g, half);
-                if (ha < p.G) po[ha * D + d] = o[i][2 * half] * p.v_scale;
-                if (hb < p.G) po[hb * D + d] = o[i][2 * half + 1] * p.v_scale;
+            for (int i = 0; i < D / 16; ++i) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int d = out_dim<D, FP8>(i, g, half);
+                    if (ha < sg.rows) po[ha * D + d] = o[r][i][2 * half] * p.v_scale;
+                    if (hb < sg.rows) po[hb * D + d] = o[r][i][2 * half + 1] * p.v_scale;
+                }
+            }
+            if (g == 0) {
+                if (ha < sg.rows) p.part_ml[slot * p.prow + ha] = make_float2(ma[r], la[r]);
+                if (hb < sg.rows) p.part_ml[slot * p.prow + hb] = make_float2(mb[r], lb[r]);
             }
         }
-        if (g == 0) {
-            if (ha < p.G) p.part_ml[slot * p.G + ha] = make_float2(ma, la);
-            if (hb < p.G) p.part_ml[slot * p.G + hb] = make_float2(mb, lb);
-        }
     }
-    if (first_blk == 0 && lane == 0) {
-        // block 0 of the pair is here: record the warps whose ranges meet its
-        // blocks [flat_first, flat_first + nb)
-        const int w_last = (flat_first + nb - 1) / q;
-        p.pair_meta[pair] = make_int2(w, w_last - w + 1);
+    if (sg.first == sg.base && lane == 0) {
+        // the stream's first block is here: record the first partial slot
+        // and the warps whose ranges meet its blocks
+        // [flat_first, flat_first + (end - base))
+        const int flat_first = b0 + sg.i0;
+        const int w_last = (flat_first + (sg.end - sg.base) - 1) / q;
+        p.pair_meta[sg.pair] = make_int4(slot_base + sg.pair + w, w_last - w + 1, sg.cj, 0);
     }
 }
 
@@ -562,10 +777,9 @@ __device__ __forceinline__ void append_patch(const DecodeParams& p, int s, int h
     __syncwarp();
 }
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, Geom<D, FP8>::MIN_CTAS)
-paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
+template <int D, bool FP8, int NR>
+__device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                           const DecodeParams& p)
 {
     using G = Geom<D, FP8>;
     constexpr int ST = G::STAGES;
@@ -589,239 +803,298 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     pdl_launch_dependents();
     pdl_wait();
 
-    // ---- 1. total work and this warp's range --------------------------------
-    constexpr int U = 8;           // first 256 sequences stay in registers
-    int nbv[U], incl[U];
-    int carry = 0;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int s = u * 32 + lane;
-        int Lc;
-        nbv[u] = s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        incl[u] = warp_incl_scan(nbv[u] * p.Hkv, lane) + carry;
-        carry = __shfl_sync(kFull, incl[u], 31);
-    }
-    int total = carry;
-    // sequences past the first 256: 256 at a time, all loads issued together
-    for (int base = U * 32; base < p.B; base += U * 32) {
-        int v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int s = base + u * 32 + lane;
-            int Lc;
-            v[u] = s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) : 0;
-        }
-        int sum = 0;
-#pragma unroll
-        for (int u = 0; u < U; ++u) sum += v[u];
-        total += warp_sum(sum) * p.Hkv;
-    }
-    if (total == 0) return;
-    int q = (total + p.warps_total - 1) / p.warps_total;
-    if (q < kMinBlocksPerWarp) q = kMinBlocksPerWarp;
-    const int weff = (total + q - 1) / q;
-    if (w >= weff) return;
-    const int b0 = w * q;
-    const int cnt = min(q, total - b0);
-
-    // ---- 2. the (sequence, head, block) where the range starts --------------
-    int s0 = -1, excl = 0;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const unsigned mball = __ballot_sync(kFull, incl[u] > b0);
-        if (s0 < 0 && mball) {
-            const int src = __ffs(mball) - 1;
-            s0 = u * 32 + src;
-            excl = __shfl_sync(kFull, incl[u] - nbv[u] * p.Hkv, src);
-        }
-    }
-    if (s0 < 0) {
-        int c2 = carry;
-        for (int base = U * 32; base < p.B && s0 < 0; base += U * 32) {
-            int v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int s = base + u * 32 + lane;
-                int Lc;
-                v[u] = s < p.B ? seq_blocks(p.ctx, s, p.max_blocks, Lc) * p.Hkv : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int inc = warp_incl_scan(v[u], lane) + c2;
-                const unsigned mball = __ballot_sync(kFull, inc > b0);
-                if (s0 < 0 && mball) {
-                    const int src = __ffs(mball) - 1;
-                    s0 = base + u * 32 + src;
-                    excl = __shfl_sync(kFull, inc - v[u], src);
-                }
-                c2 = __shfl_sync(kFull, inc, 31);
-            }
-        }
-    }
-    if (s0 < 0) return;      // unreachable with consistent input
-    int L0;
-    const int nb0 = seq_blocks(p.ctx, s0, p.max_blocks, L0);
-    const int off0 = b0 - excl;
-    const int h0 = off0 / nb0;
-    const int blk0 = off0 - h0 * nb0;
-
-    // ---- 3. pipeline set-up ---------------------------------------------------
     if (lane == 0) {
 #pragma unroll
         for (int st = 0; st < ST; ++st) mbar_init(bar0 + st * 8, 1);
         fence_mbar_init();
     }
     __syncwarp();
+    int st = 0;                   // the ring carries over from one phase to the next
+    uint32_t phase = 0;
 
-    Win cur, nxt;
-    int wb = 0;
-    fill_window(cur, p, s0, h0, blk0, nb0, L0, 0, cnt, lane);
-    nxt = cur;
-    auto refill_next = [&](int pos0) {
-        const int cs = __shfl_sync(kFull, cur.s, 31), ch = __shfl_sync(kFull, cur.h, 31);
-        const int cb = __shfl_sync(kFull, cur.blk, 31) + 1;
-        const int cL = __shfl_sync(kFull, cur.L, 31);
-        fill_window(nxt, p, cs, ch, cb, (cL + kBlock - 1) / kBlock, cL, pos0, cnt, lane);
-    };
-    if (cnt > 32) refill_next(32);
+    // Phase 0 (NR == 2 kernels with prefix chunks): the chunk streams, cut
+    // into equal per-warp ranges; phase 1: the sequence streams, likewise.
+    // Every warp takes its share of both, so the costlier chunk units do not
+    // pile up on a few warps.
+    for (int ph = (NR == 2 && p.nc > 0) ? 0 : 1; ph < 2; ++ph) {
+        const int nc = NR == 2 ? p.nc : 0;
+        const int s_lo = ph == 0 ? 0 : nc;
+        const int ns = ph == 0 ? nc : nc + p.B;           // streams [s_lo, ns)
+        const int min_q = ph == 0 ? kMinBlocksPerWarpChunk : kMinBlocksPerWarp;
+        const int slot_base = ph == 0 ? 0 : p.slot_base;
 
-    auto issue = [&](int j, int st) {
-        if (j >= wb + 32) {
-            cur = nxt;
-            wb += 32;
-            if (wb + 32 < cnt) refill_next(wb + 32);
+        // ---- 1. total work and this warp's range --------------------------------
+        constexpr int U = 8;           // first 256 streams stay in registers
+        int nbv[U], incl[U];
+        int carry = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int sg = s_lo + u * 32 + lane;
+            nbv[u] = sg < ns ? max(stream_at<NR>(p, sg).nblk, 0) : 0;
         }
-        const int src = j - wb;
-        const int id = __shfl_sync(kFull, cur.id, src);
-        const int s = __shfl_sync(kFull, cur.s, src);
-        const int h = __shfl_sync(kFull, cur.h, src);
-        const int blk = __shfl_sync(kFull, cur.blk, src);
-        const int L = __shfl_sync(kFull, cur.L, src);
-        if (lane == 0) {
-            const bool valid = id >= 0 && id < p.num_blocks;
-            const int pair = s * p.Hkv + h;
-            meta[st] = make_int4(valid ? pair : -1 - pair, blk, L, id);
-            const uint32_t bar = bar0 + st * 8;
-            const uint32_t dst = stage0 + (uint32_t)(st * G::STAGE);
-            if (valid) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar, (uint32_t)G::STAGE);
-                const int z = id * p.Hkv + h;
-                // KV tiles are read once per step: keep them from evicting
-                // the block tables, queries and partials from L2
-                const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
-                for (int b = 0; b < G::NBOX; ++b)
-                    tma_load_3d_hint(dst + b * G::BOXB, &tm_k, b * (G::BOXW / G::ES), 0, z, bar,
-                                     pol);
+        for (int u = 0; u < U; ++u) {
+            incl[u] = warp_incl_scan(nbv[u] * p.Hkv, lane) + carry;
+            carry = __shfl_sync(kFull, incl[u], 31);
+        }
+        int total = carry;
+        // streams past the first 256: 256 at a time, all loads issued together
+        for (int base = s_lo + U * 32; base < ns; base += U * 32) {
+            int v[U];
 #pragma unroll
-                for (int b = 0; b < G::NBOX; ++b)
-                    tma_load_3d_hint(dst + G::TILE + b * G::BOXB, &tm_v, b * (G::BOXW / G::ES), 0,
-                                     z, bar, pol);
-            } else {
-                raise_flag(&g_decode_err, KV_DEVERR_BLOCK_OUT_OF_RANGE, id);
-                mbar_arrive(bar);
+            for (int u = 0; u < U; ++u) {
+                const int sg = base + u * 32 + lane;
+                v[u] = sg < ns ? max(stream_at<NR>(p, sg).nblk, 0) : 0;
+            }
+            int sum = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) sum += v[u];
+            total += warp_sum(sum) * p.Hkv;
+        }
+        if (total == 0) continue;
+        int q = (total + p.warps_total - 1) / p.warps_total;
+        if (q < min_q) q = min_q;
+        const int weff = (total + q - 1) / q;
+        if (w >= weff) continue;
+        const int b0 = w * q;
+        const int cnt = min(q, total - b0);
+
+        // ---- 2. the (stream, head, block) where the range starts ----------------
+        int s0 = -1, excl = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const unsigned mball = __ballot_sync(kFull, incl[u] > b0);
+            if (s0 < 0 && mball) {
+                const int src = __ffs(mball) - 1;
+                s0 = s_lo + u * 32 + src;
+                excl = __shfl_sync(kFull, incl[u] - nbv[u] * p.Hkv, src);
             }
         }
-    };
-
-    const int npro = min(ST, cnt);
-    for (int j = 0; j < npro; ++j) issue(j, j);
-
-    // ---- 4. main loop ------------------------------------------------------------
-    // Two consecutive tiles of the same pair are consumed together where the
-    // range allows: one softmax update and one loop turn per 32 tokens.
-    uint32_t qa0[D / 16], qa2[D / 16];
-    float o[D / 16][4];
-    float m = -INFINITY, l = 0.f;
-    int seg_s = -1, seg_h = -1, seg_first = 0, seg_last = 0, seg_L = 0, seg_i0 = 0;
-    int seg_pair = -1;
-    int st = 0;
-    uint32_t phase = 0;
-    // Wait for unit i in stage `sst`; on time-out flag the error and let the
-    // copies of units [i, issued_end) land before the warp gives up.
-    auto wait_unit = [&](int i, int sst, uint32_t ph, int issued_end) -> bool {
-        bool ok = mbar_wait_bounded(bar0 + sst * 8, ph, kWaitLimit);
-        ok = __all_sync(kFull, ok);
-        if (!ok) {
-            if (lane == 0) {
-                raise_flag(&g_decode_err, KV_DEVERR_PIPELINE_TIMEOUT, i);
-                for (int j = i; j < issued_end; ++j) {
-                    mbar_wait_bounded(bar0 + sst * 8, ph, kWaitLimit);
-                    if (++sst == ST) { sst = 0; ph ^= 1u; }
+        if (s0 < 0) {
+            int c2 = carry;
+            for (int base = s_lo + U * 32; base < ns && s0 < 0; base += U * 32) {
+                int v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int sg = base + u * 32 + lane;
+                    v[u] = sg < ns ? max(stream_at<NR>(p, sg).nblk, 0) * p.Hkv : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int inc = warp_incl_scan(v[u], lane) + c2;
+                    const unsigned mball = __ballot_sync(kFull, inc > b0);
+                    if (s0 < 0 && mball) {
+                        const int src = __ffs(mball) - 1;
+                        s0 = base + u * 32 + src;
+                        excl = __shfl_sync(kFull, inc - v[u], src);
+                    }
+                    c2 = __shfl_sync(kFull, inc, 31);
                 }
             }
-            __syncwarp();
         }
-        return ok;
-    };
-    for (int i = 0; i < cnt;) {
-        const int issued_end = min(cnt, i + ST);
-        if (!wait_unit(i, st, phase, issued_end)) return;
-        const int4 mt = meta[st];
-        const bool valid = mt.x >= 0;
-        const int pair = valid ? mt.x : -1 - mt.x;
-        const int blk = mt.y, L = mt.z;
-        if (pair != seg_pair) {
-            seg_pair = pair;
-            const int s = pair / p.Hkv, h = pair - s * p.Hkv;
-            if (seg_s >= 0)
-                finalize<D, FP8>(p, w, q, seg_s, seg_h, seg_first, seg_last, seg_L, b0 + seg_i0,
-                                 m, l, o, lane);
-            seg_s = s; seg_h = h; seg_first = blk; seg_L = L; seg_i0 = i;
-            load_q<D, FP8>(p, s, h, lane, qa0, qa2);
-            m = -INFINITY;
-            l = 0.f;
-#pragma unroll
-            for (int a = 0; a < D / 16; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
-        }
-        const int st2 = st + 1 == ST ? 0 : st + 1;
-        const uint32_t phase2 = st + 1 == ST ? phase ^ 1u : phase;
-        bool two = false;
-        if (valid && i + 1 < cnt) {
-            __syncwarp();            // unit i+1's metadata was written by lane 0
-            two = meta[st2].x == mt.x;
-        }
-        const uint32_t kb = stage0 + (uint32_t)(st * G::STAGE);
-        if (two) {
-            if (!wait_unit(i + 1, st2, phase2, issued_end)) return;
-            const int id2 = meta[st2].w;
-            const uint32_t kb2 = stage0 + (uint32_t)(st2 * G::STAGE);
-            const int rest = L - (blk + 1) * kBlock;
-            const int nvalid = min(kBlock, rest);
-            if (p.k_new != nullptr && nvalid == rest)     // the pair's last block
-                append_patch<D, FP8>(p, seg_s, seg_h, id2, L, kb2, kb2 + G::TILE, lane);
-            const uint32_t kbs[2] = {kb, kb2};
-            attend_tiles<D, FP8, 2>(kbs, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
-            seg_last = blk + 1;
-            __syncwarp();
-            if (i + ST < cnt) issue(i + ST, st);
-            if (i + 1 + ST < cnt) issue(i + 1 + ST, st2);
-            st = st2 + 1 == ST ? 0 : st2 + 1;
-            phase = st2 + 1 == ST ? phase2 ^ 1u : phase2;
-            i += 2;
-        } else {
-            seg_last = blk;
-            if (valid) {
-                const int nvalid = min(kBlock, L - blk * kBlock);
-                if (p.k_new != nullptr && nvalid == L - blk * kBlock)     // the pair's last block
-                    append_patch<D, FP8>(p, seg_s, seg_h, mt.w, L, kb, kb + G::TILE, lane);
-                const uint32_t kbs[1] = {kb};
-                attend_tiles<D, FP8, 1>(kbs, nvalid, qa0, qa2, p.sl2, m, l, o, lane);
+        if (s0 < 0) continue;      // unreachable with consistent input
+        const Stream S0 = stream_at<NR>(p, s0);
+        if (S0.nblk <= 0) continue;     // inputs changed under the launch
+        const int off0 = b0 - excl;
+        const int h0 = off0 / S0.nblk;
+        const int j0 = off0 - h0 * S0.nblk;
+
+        // ---- 3. block-id windows and the copy issue -------------------------------
+        Win cur, nxt;
+        int wb = 0;
+        fill_window<NR>(cur, p, ns, s0, h0, j0, S0, 0, cnt, lane);
+        nxt = cur;
+        auto refill_next = [&](int pos0) {
+            const int cs = __shfl_sync(kFull, cur.s, 31), ch = __shfl_sync(kFull, cur.h, 31);
+            const int cb = __shfl_sync(kFull, cur.blk, 31) + 1;
+            // the stream of the window's last entry, from registers (no loads)
+            Stream S;
+            S.L = __shfl_sync(kFull, cur.L, 31);
+            S.base = NR == 2 ? __shfl_sync(kFull, cur.base, 31) : 0;
+            S.row = NR == 2 ? __shfl_sync(kFull, cur.row, 31) : cs;
+            S.nblk = (S.L + kBlock - 1) / kBlock - S.base;
+            S.cj = -1;
+            fill_window<NR>(nxt, p, ns, cs, ch, cb - S.base, S, pos0, cnt, lane);
+        };
+        if (cnt > 32) refill_next(32);
+
+        // unit j (of this phase's range) into ring stage `sst`
+        auto issue = [&](int j, int sst) {
+            if (j >= wb + 32) {
+                cur = nxt;
+                wb += 32;
+                if (wb + 32 < cnt) refill_next(wb + 32);
             }
-            __syncwarp();
-            if (i + ST < cnt) issue(i + ST, st);
-            st = st2;
-            phase = phase2;
-            i += 1;
+            const int src = j - wb;
+            const int id = __shfl_sync(kFull, cur.id, src);
+            const int s = __shfl_sync(kFull, cur.s, src);
+            const int h = __shfl_sync(kFull, cur.h, src);
+            const int blk = __shfl_sync(kFull, cur.blk, src);
+            const int L = __shfl_sync(kFull, cur.L, src);
+            if (lane == 0) {
+                const bool valid = id >= 0 && id < p.num_blocks;
+                const int pair = s * p.Hkv + h;
+                meta[sst] = make_int4(valid ? pair : -1 - pair, blk, L, id);
+                const uint32_t bar = bar0 + sst * 8;
+                const uint32_t dst = stage0 + (uint32_t)(sst * G::STAGE);
+                if (valid) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar, (uint32_t)G::STAGE);
+                    const int z = id * p.Hkv + h;
+                    // KV tiles are read once per step: keep them from evicting
+                    // the block tables, queries and partials from L2
+                    const uint64_t pol = l2_evict_first_policy();
+#pragma unroll
+                    for (int b = 0; b < G::NBOX; ++b)
+                        tma_load_3d_hint(dst + b * G::BOXB, &tm_k, b * (G::BOXW / G::ES), 0, z,
+                                         bar, pol);
+#pragma unroll
+                    for (int b = 0; b < G::NBOX; ++b)
+                        tma_load_3d_hint(dst + G::TILE + b * G::BOXB, &tm_v,
+                                         b * (G::BOXW / G::ES), 0, z, bar, pol);
+                } else {
+                    raise_flag(&g_decode_err, KV_DEVERR_BLOCK_OUT_OF_RANGE, id);
+                    mbar_arrive(bar);
+                }
+            }
+        };
+
+        {
+            int sst = st;
+            const int npro = min(ST, cnt);
+            for (int j = 0; j < npro; ++j) {
+                issue(j, sst);
+                if (++sst == ST) sst = 0;
+            }
         }
+
+        // ---- 4. main loop ------------------------------------------------------------
+        // Two consecutive tiles of a sequence stream are consumed together
+        // where the range allows: one softmax update and one loop turn per 32
+        // tokens.  (Prefix chunk segments take one tile per update: a second
+        // inlined copy of their two-row-tile math costs more than it saves.)
+        QFrag<D> qf;
+        float o[NR][D / 16][4];
+        float m[NR], l[NR];
+        Seg sg;
+        sg.pair = -1;
+        bool open = false;
+        // Wait for unit i in stage `sst`; on time-out flag the error and let the
+        // copies of units [i, issued_end) land before the warp gives up.
+        auto wait_unit = [&](int i, int sst, uint32_t phs, int issued_end) -> bool {
+            bool ok = mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
+            ok = __all_sync(kFull, ok);
+            if (!ok) {
+                if (lane == 0) {
+                    raise_flag(&g_decode_err, KV_DEVERR_PIPELINE_TIMEOUT, i);
+                    for (int j = i; j < issued_end; ++j) {
+                        mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
+                        if (++sst == ST) { sst = 0; phs ^= 1u; }
+                    }
+                }
+                __syncwarp();
+            }
+            return ok;
+        };
+        for (int i = 0; i < cnt;) {
+            const int issued_end = min(cnt, i + ST);
+            if (!wait_unit(i, st, phase, issued_end)) return;
+            const int4 mt = meta[st];
+            const bool valid = mt.x >= 0;
+            const int pair = valid ? mt.x : -1 - mt.x;
+            const int blk = mt.y, L = mt.z;
+            if (pair != sg.pair) {
+                if (open) finalize<D, FP8, NR>(p, w, q, b0, slot_base, sg, m, l, o, lane);
+                open = true;
+                const int sig = pair / p.Hkv;
+                const Stream S = stream_at<NR>(p, sig);
+                sg.pair = pair;
+                sg.h = pair - sig * p.Hkv;
+                sg.chunk = NR == 2 && sig < nc;
+                sg.s = sg.chunk ? sig : sig - nc;
+                sg.rows = p.G;
+                if (sg.chunk)
+                    sg.rows = p.G * __ldg(p.chunk + (size_t)sig * KV_PREFIX_CHUNK_INTS + 1);
+                sg.nr = NR == 2 && sg.rows > 8 ? 2 : 1;
+                sg.base = S.base;
+                sg.end = S.base + S.nblk;
+                sg.cj = S.cj;
+                sg.first = blk;
+                sg.i0 = i;
+                load_q<D, FP8, NR>(p, sg.chunk, sg.s, sg.h, sg.rows, lane, qf);
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    m[r] = -INFINITY;
+                    l[r] = 0.f;
+#pragma unroll
+                    for (int a = 0; a < D / 16; ++a)
+                        o[r][a][0] = o[r][a][1] = o[r][a][2] = o[r][a][3] = 0.f;
+                }
+            }
+            const int st2 = st + 1 == ST ? 0 : st + 1;
+            const uint32_t phase2 = st + 1 == ST ? phase ^ 1u : phase;
+            bool two = false;
+            if (!sg.chunk && valid && i + 1 < cnt) {
+                __syncwarp();            // unit i+1's metadata was written by lane 0
+                two = meta[st2].x == mt.x;
+            }
+            const uint32_t kb = stage0 + (uint32_t)(st * G::STAGE);
+            // the fused append writes the new token into its sequence's last block
+            const bool own_last = !sg.chunk && p.k_new != nullptr;
+            if (two) {
+                if (!wait_unit(i + 1, st2, phase2, issued_end)) return;
+                const int id2 = meta[st2].w;
+                const uint32_t kb2 = stage0 + (uint32_t)(st2 * G::STAGE);
+                const int rest = L - (blk + 1) * kBlock;
+                const int nvalid = min(kBlock, rest);
+                if (own_last && nvalid == rest)
+                    append_patch<D, FP8>(p, sg.s, sg.h, id2, L, kb2, kb2 + G::TILE, lane);
+                const uint32_t kbs[2] = {kb, kb2};
+                attend<D, FP8, 2, NR>(sg.nr, kbs, nvalid, qf, p.sl2, m, l, o, lane);
+                sg.last = blk + 1;
+                __syncwarp();
+                if (i + ST < cnt) issue(i + ST, st);
+                if (i + 1 + ST < cnt) issue(i + 1 + ST, st2);
+                st = st2 + 1 == ST ? 0 : st2 + 1;
+                phase = st2 + 1 == ST ? phase2 ^ 1u : phase2;
+                i += 2;
+            } else {
+                sg.last = blk;
+                if (valid) {
+                    const int nvalid = min(kBlock, L - blk * kBlock);
+                    if (own_last && nvalid == L - blk * kBlock)
+                        append_patch<D, FP8>(p, sg.s, sg.h, mt.w, L, kb, kb + G::TILE, lane);
+                    const uint32_t kbs[1] = {kb};
+                    attend<D, FP8, 1, NR>(sg.nr, kbs, nvalid, qf, p.sl2, m, l, o, lane);
+                }
+                __syncwarp();
+                if (i + ST < cnt) issue(i + ST, st);
+                st = st2;
+                phase = phase2;
+                i += 1;
+            }
+        }
+        if (open) finalize<D, FP8, NR>(p, w, q, b0, slot_base, sg, m, l, o, lane);
     }
-    if (seg_s >= 0)
-        finalize<D, FP8>(p, w, q, seg_s, seg_h, seg_first, seg_last, seg_L, b0 + seg_i0, m, l, o,
-                         lane);
+}
+
+// Plain decoding: one row tile per unit.
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kWarps * 32, Geom<D, FP8>::MIN_CTAS)
+paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
+{
+    split_body<D, FP8, 1>(tm_k, tm_v, p);
+}
+
+// Shared-prefix decoding: prefix chunks with up to 16 query rows, then the
+// sequences.
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kWarps * 32, Geom<D, FP8>::MIN_CTAS)
+paged_decode_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
+{
+    split_body<D, FP8, 2>(tm_k, tm_v, p);
 }
 
 // -------------------------------------------------------------------- merge
@@ -831,45 +1104,78 @@ struct MergeParams {
     const int32_t* ctx;
     const float* part_o;
     const float2* part_ml;
-    const int2* pair_meta;
+    const int4* pair_meta;
+    const int32_t* chunk;    // prefix chunks (checked here, read by the split kernel)
+    const int32_t* seq_chunk;
+    int nc;
     int B, Hq, Hkv, G, max_blocks;
+    int prow;                // rows per partial slot
     int nslots;              // partial slots in the workspace
     int out_f32;
 };
 
 // One CTA per (sequence, KV head): merge the partials the split kernel left
-// for it (pairs seen whole by one warp were written there already), or write
-// zeros for an empty context.  Thread t owns output float4 column t of the
-// pair's G x D block; the (max, sum) terms of up to 64 partials at a time go
-// through shared memory, and a thread's partial loads are independent of one
-// another, so the merge costs a few L2 round trips.
-constexpr int kMergeThreads = 256;   // >= 8 heads x 128 / 4 columns
+// for it -- those of its own blocks and, with a shared prefix, its rows of
+// the prefix chunk's partials -- (a sequence seen whole by one warp was
+// written there already), or write zeros for an empty context.  Thread t
+// owns output float4 column t of the pair's G x D block; the (max, sum)
+// terms of up to 64 partials at a time go through shared memory, and a
+// thread's partial loads are independent of one another, so the merge costs
+// a few L2 round trips.
+constexpr int kMergeMaxThreads = 256;   // >= 8 heads x 128 / 4 columns
 constexpr int kMergeChunk = 64;
 
+// Threads of a merge CTA: one per float4 column of the G x D block, whole warps.
+inline int merge_threads(int G, int D) { return (G * D / 4 + 31) / 32 * 32; }
+
+// Small CTAs with few registers, so that they fit beside the split kernel's
+// CTAs and start (programmatic dependent launch) before it drains.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads, 1) paged_decode_merge_kernel(const MergeParams p)
+__global__ void __launch_bounds__(kMergeMaxThreads, 4) paged_decode_merge_kernel(const MergeParams p)
 {
     __shared__ float2 sml[kMergeChunk * 8];
     pdl_launch_dependents();
     pdl_wait();
-    const int pair = blockIdx.x;
-    const int s = pair / p.Hkv, h = pair - s * p.Hkv;
+    const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
     const int t = threadIdx.x;
+    const int nthr = blockDim.x;
     const int cols = p.G * (D / 4);
     const size_t row = (size_t)s * p.Hq + (size_t)h * p.G;
     int L;
-    seq_blocks(p.ctx, s, p.max_blocks, L);
+    seq_blocks(p.ctx, s, p.max_blocks, L, true);
+    if (p.nc > 0 && h == 0 && t == 0) {
+        // report inconsistent prefix-chunk entries (the split kernel only reads)
+        int c, j, lead, members;
+        prefix_of(p.chunk, p.seq_chunk, p.nc, p.B, p.G, p.max_blocks, s, L, c, j, true);
+        if (s < p.nc) chunk_blocks(p.chunk, s, p.B, p.G, p.max_blocks, lead, members, true);
+    }
     if (L <= 0) {
         if (t < cols) store4(p, row * D + 4 * t, 0.f, 0.f, 0.f, 0.f);
         return;
     }
-    const int2 mt = p.pair_meta[pair];
-    const int n = mt.y;
-    if (n <= 1) return;
+    const int pair = (p.nc + s) * p.Hkv + h;
+    const int4 mt = p.pair_meta[pair];
+    const int na = mt.y;
     // the table is rewritten by every split launch; refuse anything that
     // would leave the workspace (only an aborted split launch leaves it stale)
-    if (mt.x < 0 || (long long)pair + mt.x + n > (long long)p.nslots) return;
-    const size_t slot0 = (size_t)pair + mt.x;
+    if (mt.x < 0 || na < 1 || (long long)mt.x + na > (long long)p.nslots) return;
+    // the prefix chunk's partials (recorded by the split kernel): slots from
+    // cpair + w0, rows from member * G
+    int nb = 0, crow = 0;
+    long long cslot0 = 0;
+    if (mt.z >= 0 && (mt.z >> 4) < p.nc) {
+        const int cpair = (mt.z >> 4) * p.Hkv + h;
+        const int4 cm = p.pair_meta[cpair];
+        if (cm.x < 0 || cm.y < 1 || (long long)cm.x + cm.y > (long long)p.nslots ||
+            (mt.z & 15) * p.G + p.G > p.prow)
+            return;
+        nb = cm.y;
+        cslot0 = cm.x;
+        crow = (mt.z & 15) * p.G;
+    }
+    if (na <= 1 && nb == 0) return;
+    const long long aslot0 = mt.x;
+    const int n = na + nb;
     const int g = t / (D / 4), d4 = t % (D / 4);
     const bool live = t < cols;
     float M = -INFINITY, den = 0.f;
@@ -877,9 +1183,12 @@ __global__ void __launch_bounds__(kMergeThreads, 1) paged_decode_merge_kernel(co
     for (int k0 = 0; k0 < n; k0 += kMergeChunk) {
         const int nk = min(kMergeChunk, n - k0);
         __syncthreads();
-        for (int i = t; i < nk * p.G; i += kMergeThreads) {
+        for (int i = t; i < nk * p.G; i += nthr) {
             const int kk = i / p.G, gg = i - kk * p.G;
-            float2 v = __ldcg(&p.part_ml[(slot0 + k0 + kk) * p.G + gg]);
+            const int k = k0 + kk;
+            const size_t r = k < na ? (size_t)(aslot0 + k) * p.prow + gg
+                                    : (size_t)(cslot0 + (k - na)) * p.prow + crow + gg;
+            float2 v = __ldcg(&p.part_ml[r]);
             if (!(v.y > 0.f)) v = make_float2(-INFINITY, 0.f);     // empty partial
             sml[kk * 8 + gg] = v;
         }
@@ -892,12 +1201,13 @@ __global__ void __launch_bounds__(kMergeThreads, 1) paged_decode_merge_kernel(co
         den *= r;
         acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
         M = Mn;
-        const float4* po = reinterpret_cast<const float4*>(p.part_o + (slot0 + k0) * p.G * D) +
-                           (size_t)g * (D / 4) + d4;
-#pragma unroll 8
-        for (int k = 0; k < nk; ++k) {
-            const float4 o = __ldcg(po + (size_t)k * p.G * (D / 4));
-            const float2 v = sml[k * 8 + g];
+#pragma unroll 4
+        for (int kk = 0; kk < nk; ++kk) {
+            const int k = k0 + kk;
+            const size_t prw = k < na ? (size_t)(aslot0 + k) * p.prow + g
+                                      : (size_t)(cslot0 + (k - na)) * p.prow + crow + g;
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + prw * D) + d4);
+            const float2 v = sml[kk * 8 + g];
             const float f = v.y > 0.f ? exp2f(v.x - M) : 0.f;
             den += f * v.y;
             acc.x += f * o.x;
@@ -926,24 +1236,25 @@ struct VariantInfo {
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    VariantInfo v[2][2];    // [D==128][fp8]
+    VariantInfo v[2][2][2];    // [D==128][fp8][NR==2]
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NR>
 const void* split_fn()
 {
+    if constexpr (NR == 2) return reinterpret_cast<const void*>(&paged_decode_prefix_kernel<D, FP8>);
     return reinterpret_cast<const void*>(&paged_decode_split_kernel<D, FP8>);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NR>
 int variant_setup(VariantInfo& vi)
 {
     using G = Geom<D, FP8>;
-    const void* fn = split_fn<D, FP8>();
+    const void* fn = split_fn<D, FP8, NR>();
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM) !=
         cudaSuccess)
         return KV_ERR_CUDA;
@@ -957,8 +1268,14 @@ int variant_setup(VariantInfo& vi)
     return KV_OK;
 }
 
+template <int D, bool FP8>
+int variant_setup_nr(VariantInfo& vi, int nr)
+{
+    return nr == 2 ? variant_setup<D, FP8, 2>(vi) : variant_setup<D, FP8, 1>(vi);
+}
+
 // Device facts and per-variant occupancy, cached per device.
-int device_info(int D, bool fp8, int& sms, int& ctas_per_sm)
+int device_info(int D, bool fp8, int nr, int& sms, int& ctas_per_sm)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KV_ERR_CUDA;
@@ -969,11 +1286,13 @@ int device_info(int D, bool fp8, int& sms, int& ctas_per_sm)
             return KV_ERR_CUDA;
         di.ready = true;
     }
-    VariantInfo& vi = di.v[D == 128][fp8];
+    VariantInfo& vi = di.v[D == 128][fp8][nr == 2];
     if (!vi.ready) {
         int rc;
-        if (D == 128) rc = fp8 ? variant_setup<128, true>(vi) : variant_setup<128, false>(vi);
-        else rc = fp8 ? variant_setup<64, true>(vi) : variant_setup<64, false>(vi);
+        if (D == 128)
+            rc = fp8 ? variant_setup_nr<128, true>(vi, nr) : variant_setup_nr<128, false>(vi, nr);
+        else
+            rc = fp8 ? variant_setup_nr<64, true>(vi, nr) : variant_setup_nr<64, false>(vi, nr);
         if (rc != KV_OK) return rc;
     }
     sms = di.sms;
@@ -1024,15 +1343,19 @@ struct WsLayout {
     size_t part_o, part_ml, meta, total;
 };
 
-WsLayout ws_layout(int B, int Hq, int Hkv, int D, int warps_total)
+// Partial slots: one per (stream, KV head) plus one per warp (a warp's
+// partial of pair x goes to slot x + w).  nr == 2 (prefix chunks) gives
+// slots of KV_PREFIX_MAX_ROWS rows, otherwise G rows.
+WsLayout ws_layout(int B, int nc, int Hq, int Hkv, int D, int warps_total, int nr)
 {
-    const int G = Hq / Hkv;
-    const size_t slots = (size_t)B * Hkv + (size_t)warps_total;
+    const int prow = nr == 2 ? KV_PREFIX_MAX_ROWS : Hq / Hkv;
+    const size_t pairs = ((size_t)B + (size_t)nc) * Hkv;
+    const size_t slots = pairs + (size_t)warps_total;
     WsLayout L;
     L.part_o = 0;
-    L.part_ml = align256(slots * G * D * sizeof(float));
-    L.meta = L.part_ml + align256(slots * G * sizeof(float2));
-    L.total = L.meta + align256((size_t)B * Hkv * sizeof(int2));
+    L.part_ml = align256(slots * prow * D * sizeof(float));
+    L.meta = L.part_ml + align256(slots * prow * sizeof(float2));
+    L.total = L.meta + align256(pairs * sizeof(int4));
     return L;
 }
 
@@ -1074,14 +1397,31 @@ struct AppendArgs {
     void* v_cache;
 };
 
+struct PrefixArgs {
+    const int32_t* chunk;
+    const int32_t* seq_chunk;
+    int nc;
+};
+
+template <int D, bool FP8>
+cudaError_t launch_split(int nr, unsigned grid, cudaStream_t st, const CUtensorMap& mk,
+                         const CUtensorMap& mv, const DecodeParams& dp)
+{
+    if (nr == 2)
+        return launch_pdl(paged_decode_prefix_kernel<D, FP8>, grid, kWarps * 32,
+                          Geom<D, FP8>::SMEM, st, mk, mv, dp);
+    return launch_pdl(paged_decode_split_kernel<D, FP8>, grid, kWarps * 32, Geom<D, FP8>::SMEM,
+                      st, mk, mv, dp);
+}
+
 // Validate, build the tensor maps and launch the decode kernel (one launch).
 int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
                   const void* v_cache, int kv_dtype, float k_scale, float v_scale, int num_blocks,
                   const int32_t* block_tables, int max_blocks_per_seq,
                   const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                   int head_dim, float scale, void* workspace, size_t workspace_bytes,
-                  void* stream, const AppendArgs* app, void* ev_begin, void* ev_split,
-                  void* ev_end)
+                  void* stream, const AppendArgs* app, const PrefixArgs* pre, void* ev_begin,
+                  void* ev_split, void* ev_end)
 {
     if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
     if (out_dtype != KV_DTYPE_BF16 && out_dtype != KV_DTYPE_F32) return KV_ERR_UNSUPPORTED;
@@ -1096,20 +1436,28 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
                 (((uintptr_t)app->k_new | (uintptr_t)app->v_new) & 15) != 0))
         return KV_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+    const int nc = pre ? pre->nc : 0;
+    if (nc < 0 || nc > num_seqs / 2) return KV_ERR_INVALID_ARG;
+    if (nc > 0 && (!pre->chunk || !pre->seq_chunk)) return KV_ERR_INVALID_ARG;
+    const int nr = nc > 0 ? 2 : 1;
     const bool fp8 = kv_dtype == KV_DTYPE_FP8_E4M3;
     if (fp8 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
         return KV_ERR_INVALID_ARG;
     // flat work indices and tensor-map rows must fit in int32
-    if ((long long)num_seqs * max_blocks_per_seq * num_kv_heads >= INT_MAX ||
+    if (((long long)num_seqs + nc) * max_blocks_per_seq * num_kv_heads >= INT_MAX ||
         (long long)num_blocks * num_kv_heads >= INT_MAX ||
         (long long)max_blocks_per_seq * kBlock >= INT_MAX)
         return KV_ERR_UNSUPPORTED;
 
+    // one launch: the 16-row kernel (prefix chunks, then sequences) or the
+    // plain one; with chunks each phase has its own partial slots
     int sms = 0, cps = 0;
-    if (int rc = device_info(head_dim, fp8, sms, cps)) return rc;
+    if (int rc = device_info(head_dim, fp8, nr, sms, cps)) return rc;
     const int grid = sms * cps;
     const int warps_total = grid * kWarps;
-    const WsLayout ws = ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, warps_total);
+    const int slot_warps = nr == 2 ? 2 * warps_total : warps_total;
+    const WsLayout ws =
+        ws_layout(num_seqs, nc, num_q_heads, num_kv_heads, head_dim, slot_warps, nr);
     if (workspace_bytes < ws.total) return KV_ERR_INVALID_ARG;
 
     CUtensorMap mk, mv;
@@ -1124,7 +1472,7 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.ctx = context_lens;
     dp.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
     dp.part_ml = reinterpret_cast<float2*>(wsb + ws.part_ml);
-    dp.pair_meta = reinterpret_cast<int2*>(wsb + ws.meta);
+    dp.pair_meta = reinterpret_cast<int4*>(wsb + ws.meta);
     dp.k_new = app ? static_cast<const uint16_t*>(app->k_new) : nullptr;
     dp.v_new = app ? static_cast<const uint16_t*>(app->v_new) : nullptr;
     dp.k_cache = app ? static_cast<uint8_t*>(app->k_cache) : nullptr;
@@ -1141,27 +1489,22 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.k_qscale = k_scale;
     dp.v_qscale = v_scale;
     dp.out_f32 = out_dtype == KV_DTYPE_F32;
+    dp.chunk = nc > 0 ? pre->chunk : nullptr;
+    dp.seq_chunk = nc > 0 ? pre->seq_chunk : nullptr;
+    dp.nc = nc;
+    dp.prow = nr == 2 ? KV_PREFIX_MAX_ROWS : dp.G;
+    dp.slot_base = nr == 2 ? warps_total : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (ev_begin && cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), st) != cudaSuccess)
         return KV_ERR_CUDA;
-    const int threads = kWarps * 32;
     cudaError_t err;
-    if (head_dim == 128) {
-        if (fp8)
-            err = launch_pdl(paged_decode_split_kernel<128, true>, grid, threads,
-                             Geom<128, true>::SMEM, st, mk, mv, dp);
-        else
-            err = launch_pdl(paged_decode_split_kernel<128, false>, grid, threads,
-                             Geom<128, false>::SMEM, st, mk, mv, dp);
-    } else {
-        if (fp8)
-            err = launch_pdl(paged_decode_split_kernel<64, true>, grid, threads,
-                             Geom<64, true>::SMEM, st, mk, mv, dp);
-        else
-            err = launch_pdl(paged_decode_split_kernel<64, false>, grid, threads,
-                             Geom<64, false>::SMEM, st, mk, mv, dp);
-    }
+    if (head_dim == 128)
+        err = fp8 ? launch_split<128, true>(nr, grid, st, mk, mv, dp)
+                  : launch_split<128, false>(nr, grid, st, mk, mv, dp);
+    else
+        err = fp8 ? launch_split<64, true>(nr, grid, st, mk, mv, dp)
+                  : launch_split<64, false>(nr, grid, st, mk, mv, dp);
     if (err != cudaSuccess) return KV_ERR_CUDA;
     if (ev_split && cudaEventRecord(static_cast<cudaEvent_t>(ev_split), st) != cudaSuccess)
         return KV_ERR_CUDA;
@@ -1172,17 +1515,22 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     mp.part_o = dp.part_o;
     mp.part_ml = dp.part_ml;
     mp.pair_meta = dp.pair_meta;
+    mp.chunk = dp.chunk;
+    mp.seq_chunk = dp.seq_chunk;
+    mp.nc = nc;
+    mp.prow = dp.prow;
     mp.B = num_seqs;
     mp.Hq = num_q_heads;
     mp.Hkv = num_kv_heads;
     mp.G = dp.G;
     mp.max_blocks = max_blocks_per_seq;
-    mp.nslots = num_seqs * num_kv_heads + warps_total;
+    mp.nslots = (num_seqs + nc) * num_kv_heads + slot_warps;
     mp.out_f32 = dp.out_f32;
     const unsigned mgrid = (unsigned)(num_seqs * num_kv_heads);
+    const unsigned mthreads = (unsigned)merge_threads(dp.G, head_dim);
     err = head_dim == 128
-              ? launch_pdl(paged_decode_merge_kernel<128>, mgrid, kMergeThreads, 0, st, mp)
-              : launch_pdl(paged_decode_merge_kernel<64>, mgrid, kMergeThreads, 0, st, mp);
+              ? launch_pdl(paged_decode_merge_kernel<128>, mgrid, mthreads, 0, st, mp)
+              : launch_pdl(paged_decode_merge_kernel<64>, mgrid, mthreads, 0, st, mp);
     if (err != cudaSuccess) return KV_ERR_CUDA;
     if (ev_end && cudaEventRecord(static_cast<cudaEvent_t>(ev_end), st) != cudaSuccess)
         return KV_ERR_CUDA;
@@ -1254,9 +1602,46 @@ extern "C" int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int n
     *bytes = 0;
     if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
     int sms = 0, cps = 0;
-    if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, sms, cps)) return rc;
-    *bytes = ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, sms * cps * kWarps).total;
+    if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, 1, sms, cps)) return rc;
+    *bytes = ws_layout(num_seqs, 0, num_q_heads, num_kv_heads, head_dim, sms * cps * kWarps, 1)
+                 .total;
     return KV_OK;
+}
+
+extern "C" int paged_decode_prefix_workspace_bytes(int num_seqs, int num_chunks, int num_q_heads,
+                                                   int num_kv_heads, int head_dim, int kv_dtype,
+                                                   size_t* bytes)
+{
+    if (!bytes) return KV_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
+    if (num_chunks < 0 || num_chunks > num_seqs / 2) return KV_ERR_INVALID_ARG;
+    const int nr = num_chunks > 0 ? 2 : 1;
+    int sms = 0, cps = 0;
+    if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, nr, sms, cps)) return rc;
+    *bytes = ws_layout(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
+                       sms * cps * kWarps * nr, nr)
+                 .total;
+    return KV_OK;
+}
+
+extern "C" int paged_decode_prefix(void* out, int out_dtype, const void* q, const void* k_new,
+                                   const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                                   float k_scale, float v_scale, int num_blocks,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, float scale,
+                                   const int32_t* chunks, const int32_t* seq_chunk,
+                                   int num_chunks, void* workspace, size_t workspace_bytes,
+                                   void* stream)
+{
+    if ((k_new == nullptr) != (v_new == nullptr)) return KV_ERR_INVALID_ARG;
+    const AppendArgs app = {k_new, v_new, k_cache, v_cache};
+    const PrefixArgs pre = {chunks, seq_chunk, num_chunks};
+    return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                         num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                         stream, k_new ? &app : nullptr, &pre, nullptr, nullptr, nullptr);
 }
 
 extern "C" int paged_decode_attention_timed(
@@ -1269,7 +1654,7 @@ extern "C" int paged_decode_attention_timed(
     return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                          num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
-                         stream, nullptr, ev_begin, ev_split_end, ev_end);
+                         stream, nullptr, nullptr, ev_begin, ev_split_end, ev_end);
 }
 
 extern "C" int paged_decode_attention(void* out, int out_dtype, const void* q, const void* k_cache,
@@ -1283,7 +1668,7 @@ extern "C" int paged_decode_attention(void* out, int out_dtype, const void* q, c
     return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                          num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
-                         stream, nullptr, nullptr, nullptr, nullptr);
+                         stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
 extern "C" int paged_decode_step(void* out, int out_dtype, const void* q, const void* k_new,
@@ -1298,7 +1683,7 @@ extern "C" int paged_decode_step(void* out, int out_dtype, const void* q, const 
     return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                          num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
-                         stream, &app, nullptr, nullptr, nullptr);
+                         stream, &app, nullptr, nullptr, nullptr, nullptr);
 }
 
 extern "C" int kv_get_device_error(int* flags, int64_t* detail)

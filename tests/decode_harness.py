@@ -30,10 +30,11 @@ def half_ulp_bf16(x):
 
 
 def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None, stream=None,
-             fused=False, workspace=None):
+             fused=False, workspace=None, prefix=None):
     """Returns (out, k_cache, v_cache) on the device.  fused=False: kv_append
     then paged_decode_attention (two launches); fused=True: paged_decode_step
-    (append and attention in one launch)."""
+    (append and attention in one launch).  prefix=(chunks, seq_chunk) (host
+    int32 arrays) runs the shared-prefix entry point instead."""
     import paged_kv_cache_21_gb300 as pk
     NB, Hkv, D = case.num_blocks, case.Hkv, case.D
     cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
@@ -47,10 +48,30 @@ def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None,
     pk.kv_append(pool_k, pool_v, kc, vc, all_slots, case.k_scale, case.v_scale, stream=stream)
     del pool_k, pool_v
     out = torch.empty((case.B, case.Hq, D), dtype=out_dtype, device=device)
-    ws = workspace if workspace is not None else pk.alloc_workspace(
-        case.B, case.Hq, Hkv, D, case.kv_dtype, device=device)
     bt = torch.from_numpy(case.block_tables).to(device)
     cl = torch.from_numpy(case.context_lens).to(device)
+    if prefix is not None:
+        chunks, seq_chunk = prefix
+        ws = workspace if workspace is not None else pk.alloc_prefix_workspace(
+            case.B, len(chunks), case.Hq, Hkv, D, case.kv_dtype, device=device)
+        dch = torch.from_numpy(np.ascontiguousarray(chunks, dtype=np.int32)).to(device)
+        dsc = torch.from_numpy(np.ascontiguousarray(seq_chunk, dtype=np.int32)).to(device)
+        if fused:
+            pk.paged_decode_prefix(out, case.q.to(device), kc, vc, bt, cl, dch, dsc, case.scale,
+                                   ws, case.k_scale, case.v_scale, k_new=case.k_new.to(device),
+                                   v_new=case.v_new.to(device), stream=stream)
+        else:
+            slots_new = pk.slot_mapping(case.block_tables,
+                                        case.context_lens.astype(np.int64) - 1)
+            pk.kv_append(case.k_new.to(device), case.v_new.to(device), kc, vc,
+                         torch.from_numpy(slots_new).to(device), case.k_scale, case.v_scale,
+                         stream=stream)
+            pk.paged_decode_prefix(out, case.q.to(device), kc, vc, bt, cl, dch, dsc, case.scale,
+                                   ws, case.k_scale, case.v_scale, stream=stream)
+        torch.cuda.synchronize()
+        return out, kc, vc
+    ws = workspace if workspace is not None else pk.alloc_workspace(
+        case.B, case.Hq, Hkv, D, case.kv_dtype, device=device)
     if fused:
         pk.paged_decode_step(out, case.q.to(device), case.k_new.to(device),
                              case.v_new.to(device), kc, vc, bt, cl, case.scale, ws,

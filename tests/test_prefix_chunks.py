@@ -1,0 +1,130 @@
+"""Host logic of shared-prefix decoding: the chunk table kv_prefix_chunks
+builds from block tables ("KV cache complete guide", sections "(3) Prefix
+Caching" and "(4) PagedAttention": requests with the same system prompt share
+its physical blocks).  Checked against the rules the kernels rely on, not
+against a second implementation."""
+import numpy as np
+import pytest
+
+import workloads
+
+MAX_ROWS = 16
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import __graft_entry__
+    __graft_entry__.build_native()
+    import paged_kv_cache_21_gb300 as m
+    return m
+
+
+def check_table(bt, lens, G, chunks, seq_chunk, min_blocks=1):
+    """Every rule of the chunk table: sizes, membership, sharing, and the new
+    token lying past the shared blocks."""
+    B = bt.shape[0]
+    assert seq_chunk.shape == (B,)
+    seen = set()
+    for c, row in enumerate(chunks):
+        P, m = int(row[0]), int(row[1])
+        members = [int(x) for x in row[2:2 + m]]
+        assert 2 <= m <= MAX_ROWS // G and m * G <= MAX_ROWS
+        assert all(x == -1 for x in row[2 + m:])
+        assert P >= min_blocks
+        assert len(set(members)) == m and not (set(members) & seen)
+        seen |= set(members)
+        for j, s in enumerate(members):
+            assert 0 <= s < B
+            assert seq_chunk[s] == (c << 4) | j
+            assert 16 * P <= int(lens[s]) - 1          # shared blocks end before the new token
+            np.testing.assert_array_equal(bt[s, :P], bt[members[0], :P])
+    for s in range(B):
+        if s not in seen:
+            assert seq_chunk[s] == -1
+
+
+def saved_reads(chunks):
+    return sum(int(r[0]) * (int(r[1]) - 1) for r in chunks)
+
+
+@pytest.mark.parametrize("B", [32, 256])
+def test_config3_tables(pk, B):
+    case = workloads.make_case("3", override={"B": B})
+    G = case.Hq // case.Hkv
+    chunks, seq_chunk = pk.prefix_chunks(case.block_tables, case.context_lens, G)
+    check_table(case.block_tables, case.context_lens, G, chunks, seq_chunk)
+    assert len(chunks) > 0
+    # the recipe shares min(38, N // 16) leading blocks within each group of 8:
+    # the redundant reads are sum(shared) - (one copy per group)
+    groups = B // 8
+    shared = case.shared_blocks.astype(np.int64)
+    redundant = int(shared.sum()) - sum(int(shared[8 * g:8 * g + 8].max()) for g in range(groups))
+    assert 0 < saved_reads(chunks) <= redundant
+    assert saved_reads(chunks) >= 0.5 * redundant
+
+
+def test_no_sharing_gives_no_chunks(pk):
+    case = workloads.make_custom(12, 32, 8, 128, [40 + 37 * i for i in range(12)], seed=3)
+    chunks, seq_chunk = pk.prefix_chunks(case.block_tables, case.context_lens, 4)
+    assert chunks.shape == (0, 18) and (seq_chunk == -1).all()
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 7, 8])
+def test_chunk_rows_fit_one_tile(pk, G):
+    # 20 sequences sharing 6 blocks, lengths 100..290 tokens
+    B, mb = 20, 24
+    rng = np.random.default_rng(G)
+    lens = (100 + 10 * np.arange(B)).astype(np.int32)
+    bt = np.full((B, mb), -1, dtype=np.int32)
+    ids = rng.permutation(1000).astype(np.int32)
+    shared, cur = ids[:6], 6
+    for s in range(B):
+        nb = -(-int(lens[s]) // 16)
+        bt[s, :6] = shared
+        bt[s, 6:nb] = ids[cur:cur + nb - 6]
+        cur += nb - 6
+    chunks, seq_chunk = pk.prefix_chunks(bt, lens, G)
+    check_table(bt, lens, G, chunks, seq_chunk)
+    per = MAX_ROWS // G
+    assert len(chunks) == B // per + (1 if B % per >= 2 else 0)
+    assert all(int(r[0]) == 6 for r in chunks)
+
+
+def test_nested_prefixes_and_short_members(pk):
+    # a tree: all 8 share 4 blocks, the first 4 share 10; sequence 7 has only
+    # 3 full blocks before its new token (so it shares 3), sequence 6 is empty
+    B, mb = 8, 16
+    bt = np.full((B, mb), -1, dtype=np.int32)
+    base = np.arange(100, 104, dtype=np.int32)
+    deep = np.arange(200, 206, dtype=np.int32)
+    nxt = 300
+    lens = np.array([200, 180, 190, 170, 120, 130, 0, 60], dtype=np.int32)
+    for s in range(B):
+        nb = -(-int(lens[s]) // 16)
+        if nb == 0:
+            continue
+        row = list(base) + (list(deep) if s < 4 else [])
+        row = row[:nb]
+        while len(row) < nb:
+            row.append(nxt)
+            nxt += 1
+        bt[s, :nb] = row
+    chunks, seq_chunk = pk.prefix_chunks(bt, lens, 4)
+    check_table(bt, lens, 4, chunks, seq_chunk)
+    assert seq_chunk[6] == -1
+    # the four deep members come first (run 10), then the rest (runs 4, 4, 3)
+    assert [int(x) for x in chunks[0][:2]] == [10, 4]
+    assert sorted(chunks[0][2:6].tolist()) == [0, 1, 2, 3]
+    assert [int(x) for x in chunks[1][:2]] == [3, 3]
+
+
+def test_min_blocks_and_bad_arguments(pk):
+    case = workloads.make_case("3", override={"B": 32})
+    chunks, _ = pk.prefix_chunks(case.block_tables, case.context_lens, 4, min_blocks=30)
+    assert len(chunks) > 0 and all(int(r[0]) >= 30 for r in chunks)
+    with pytest.raises(pk.KVError):
+        pk.prefix_chunks(case.block_tables, case.context_lens, 9)
+    with pytest.raises(pk.KVError):
+        pk.prefix_chunks(case.block_tables, case.context_lens, 4, min_blocks=0)
+    empty_c, empty_s = pk.prefix_chunks(np.zeros((0, 4), np.int32), np.zeros(0, np.int32), 4)
+    assert empty_c.shape[0] == 0 and empty_s.shape[0] == 0

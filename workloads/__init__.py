@@ -48,10 +48,16 @@ CONFIGS = {
                B=32, Hq=32, Hkv=8, D=128, N=8192, kv_dtype=FP8_E4M3, slack=0.10),
     "5b": dict(desc="MHA 32q/32kv heads, d128, batch 8, 4096 prefilled + 1, bf16",
                B=8, Hq=32, Hkv=32, D=128, N=4096, kv_dtype=BF16, slack=0.10),
+    # not one of the pages' workloads: config 3's structure with a long shared
+    # system prompt, where the shared blocks are most of the bytes
+    "3L": dict(desc="shared-prompt batch: 256 seqs, 32q/8kv, d128, groups of 8 sharing a "
+                    "4096-token prefix, prefilled lengths log-uniform in [4200, 8192]",
+               B=256, Hq=32, Hkv=8, D=128, N_lo=4200, N_hi=8192, group=8, prefix_blocks=256,
+               kv_dtype=BF16, slack=0.10),
 }
 
 SEED_BASE = 1000
-SEED_OFFSET = {"1": 1, "2": 2, "3": 3, "4": 4, "5a": 5, "5b": 6}
+SEED_OFFSET = {"1": 1, "2": 2, "3": 3, "4": 4, "5a": 5, "5b": 6, "3L": 7}
 
 
 @dataclass
