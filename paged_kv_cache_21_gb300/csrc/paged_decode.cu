@@ -39,6 +39,12 @@
 //    fused in: the warp that owns a pair's last block writes the new K/V to
 //    the cache and patches its own copy of that tile in shared memory before
 //    using it.
+//  * Shared prefixes (paged_decode_prefix): sequences whose block tables start
+//    with the same blocks ("KV cache complete guide", sections "(3) Prefix
+//    Caching" and "(4) PagedAttention") are cut into chunks whose query rows
+//    fill the whole 16-row MMA tile; each shared tile is read once per chunk,
+//    and the merge kernel adds each member's rows of the chunk's partials to
+//    its own.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
