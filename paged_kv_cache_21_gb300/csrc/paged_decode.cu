@@ -1130,6 +1130,7 @@ struct MergeParams {
 // a few L2 round trips.
 constexpr int kMergeMaxThreads = 256;   // >= 8 heads x 128 / 4 columns
 constexpr int kMergeChunk = 64;
+constexpr int kMergeDirect = 8;      // up to this many partials: no staging
 
 // Threads of a merge CTA: one per float4 column of the G x D block, whole warps.
 inline int merge_threads(int G, int D) { return (G * D / 4 + 31) / 32 * 32; }
@@ -1184,6 +1185,46 @@ __global__ void __launch_bounds__(kMergeMaxThreads, 4) paged_decode_merge_kernel
     const int n = na + nb;
     const int g = t / (D / 4), d4 = t % (D / 4);
     const bool live = t < cols;
+    // partial k: its row of (max, sum) and its float4 column of the output
+    auto prow_of = [&](int k) -> size_t {
+        return k < na ? (size_t)(aslot0 + k) * p.prow + g
+                      : (size_t)(cslot0 + (k - na)) * p.prow + crow + g;
+    };
+    if (n <= kMergeDirect) {
+        // few partials: every load at once (one round trip), same arithmetic
+        // and order as the staged path below
+        if (!live) return;
+        float2 v[kMergeDirect];
+        float4 ov[kMergeDirect];
+#pragma unroll
+        for (int k = 0; k < kMergeDirect; ++k) {
+            if (k < n) {
+                const size_t r = prow_of(k);
+                v[k] = __ldcg(&p.part_ml[r]);
+                ov[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D) + d4);
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMergeDirect; ++k)
+            if (k < n && v[k].y > 0.f) M = fmaxf(M, v[k].x);
+        float den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kMergeDirect; ++k) {
+            if (k < n) {
+                const float f = v[k].y > 0.f ? exp2f(v[k].x - M) : 0.f;
+                den += f * v[k].y;
+                acc.x += f * ov[k].x;
+                acc.y += f * ov[k].y;
+                acc.z += f * ov[k].z;
+                acc.w += f * ov[k].w;
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        store4(p, (row + g) * D + 4 * d4, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        return;
+    }
     float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k0 = 0; k0 < n; k0 += kMergeChunk) {
