@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "72c3a362de0fcc665cc4df4137b648ccbce4b849742e64ac239e59f9577da40d",
-           "bytes_per_launch": 1088652288,
+TRAFFIC = {"kernel_sha256": "d3395e754128b107b9d67d5cdb92e347aed9036e4f6428edf287e96264ccc39a",
+           "bytes_per_launch": 1086674944,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,144,576 B + 3,018,496 B), scaled x4 by units processed "
+                     "(269,155,328 B + 2,513,408 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 
