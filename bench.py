@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "d3395e754128b107b9d67d5cdb92e347aed9036e4f6428edf287e96264ccc39a",
-           "bytes_per_launch": 1086674944,
+TRAFFIC = {"kernel_sha256": "1d4296583efe84e5cc88794a16d9c303787b99dc8b9c1a47e90ef6bc1b8d39d3",
+           "bytes_per_launch": 1088435200,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,155,328 B + 2,513,408 B), scaled x4 by units processed "
+                     "(269,146,112 B + 2,962,688 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 
@@ -58,8 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (profiling a smaller case)")
     ap.add_argument("--prefix", action="store_true",
-                    help="also time the shared-prefix step (paged_decode_prefix with the "
-                         "chunks kv_prefix_chunks finds) beside the plain one")
+                    help="also time the shared-prefix step (paged_decode with the chunks "
+                         "kv_prefix_chunks finds) beside the plain one")
     return ap.parse_args(argv)
 
 
@@ -337,7 +337,16 @@ def run_ours(args):
     kv_bytes = case.logical_kv_bytes()
 
     def step():
-        # one decode step of the layer: append the new token and attend, one launch
+        # one decode step of the layer in a decode loop: append the new token
+        # and attend (split + merge launches); consecutive steps overlap the
+        # next step's block-table scan and first tile copies with the previous
+        # step's merge (KV_DECODE_EARLY_INPUTS: the kernel before is the
+        # previous step's, and nothing else writes the tables or the caches)
+        pk.paged_decode(out, q, kc, vc, bt, cl, case.scale, ws, case.k_scale, case.v_scale,
+                        k_new=k_new, v_new=v_new, early_inputs=True, stream=stream)
+
+    def step_default():
+        # the same step with every read after the previous kernel completes
         pk.paged_decode_step(out, q, k_new, v_new, kc, vc, bt, cl, case.scale, ws,
                              case.k_scale, case.v_scale, stream=stream)
 
@@ -399,6 +408,13 @@ def run_ours(args):
     flags, detail = pk.get_device_error()
     assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
 
+    # the same loop with the default ordering (every read after the previous
+    # kernel completes: paged_decode_step)
+    for _ in range(max(args.warmup, 3)):
+        step_default()
+    dms_local, _ = timed(K, lambda e: step_default(), 0)
+    default_step_us = reduce_max(dms_local, world, device) * 1e3
+
     # per-kernel durations: the same kernels with events around each launch
     for _ in range(max(args.warmup, 3)):
         step_split_timed([None, None, None])
@@ -419,9 +435,9 @@ def run_ours(args):
         wsp = pk.alloc_prefix_workspace(B, nc, Hq, Hkv, D, case.kv_dtype, device=device)
 
         def step_prefix():
-            pk.paged_decode_prefix(out, q, kc, vc, bt, cl, dch, dsc, case.scale, wsp,
-                                   case.k_scale, case.v_scale, k_new=k_new, v_new=v_new,
-                                   stream=stream)
+            pk.paged_decode(out, q, kc, vc, bt, cl, case.scale, wsp, case.k_scale,
+                            case.v_scale, k_new=k_new, v_new=v_new, chunks=dch, seq_chunk=dsc,
+                            early_inputs=True, stream=stream)
 
         for _ in range(max(args.warmup, 3)):
             step_prefix()
@@ -555,6 +571,8 @@ def run_ours(args):
             "config": dict(workload_config(cfg, args.batch),
                            parallelism="replicas x%d" % world if world > 1 else "single GPU"),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
+            "decode_call": "paged_decode (fused append, KV_DECODE_EARLY_INPUTS)",
+            "default_step_us": default_step_us,
             "unfused": unfused, "graph_replay": graph_replay}
     if prefix is not None:
         line["prefix"] = prefix

@@ -357,29 +357,49 @@ int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* context_lens, int num_seqs, int group_size, int min_blocks,
                      int32_t* chunks, int32_t* seq_chunk, int* num_chunks);
 
-/* Workspace bytes paged_decode_prefix needs (as paged_decode_workspace_bytes,
- * with num_chunks prefix chunks). */
+/* Workspace bytes paged_decode needs with num_chunks prefix chunks (as
+ * paged_decode_workspace_bytes, which is the num_chunks == 0 case). */
 int paged_decode_prefix_workspace_bytes(int num_seqs, int num_chunks, int num_q_heads,
                                         int num_kv_heads, int head_dim, int kv_dtype,
                                         size_t* bytes);
 
-/* Decode attention with shared prefixes: arguments as paged_decode_step,
- * plus the device copies of a chunk table and seq_chunk (above) and
- * num_chunks (0 gives plain decoding).  k_new and v_new may both be NULL:
- * then nothing is appended (as paged_decode_attention) and k_cache /
- * v_cache are only read.  A chunk entry that breaks the rules above (P out
- * of range, a member index outside [0, num_seqs), a shared block reaching a
- * member's new token, a seq_chunk entry naming another chunk) flags
- * KV_DEVERR_BAD_PREFIX; every access stays in bounds, the results of the
- * sequences concerned are undefined.  The chunk table must describe blocks
- * that really are shared: the kernel reads them from member_0's row. */
-int paged_decode_prefix(void* out, int out_dtype, const void* q, const void* k_new,
-                        const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
-                        float k_scale, float v_scale, int num_blocks, const int32_t* block_tables,
-                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
-                        int num_q_heads, int num_kv_heads, int head_dim, float scale,
-                        const int32_t* chunks, const int32_t* seq_chunk, int num_chunks,
-                        void* workspace, size_t workspace_bytes, void* stream);
+/* Flags of paged_decode. */
+#define KV_DECODE_EARLY_INPUTS 1u   /* read block_tables, context_lens, the prefix
+                                       tables and the caches early (below) */
+
+/* One decode step, general form (an interface of this implementation):
+ * arguments as paged_decode_step, plus
+ *   - k_new and v_new may both be NULL: then nothing is appended (as
+ *     paged_decode_attention) and k_cache / v_cache are only read;
+ *   - chunks, seq_chunk, num_chunks: device copies of a prefix chunk table
+ *     (above; num_chunks == 0 gives plain decoding, the tables may then be
+ *     NULL).  A chunk entry that breaks the rules above (P out of range, a
+ *     member index outside [0, num_seqs), a shared block reaching a member's
+ *     new token, a seq_chunk entry naming another chunk) flags
+ *     KV_DEVERR_BAD_PREFIX; every access stays in bounds, the results of the
+ *     sequences concerned are undefined.  The chunk table must describe
+ *     blocks that really are shared: the kernel reads them from member_0's
+ *     row;
+ *   - flags: 0 or KV_DECODE_EARLY_INPUTS.  Every kernel of this library
+ *     starts while the kernel before it on the stream drains (programmatic
+ *     dependent launch) and, by default, reads nothing until that kernel has
+ *     completed.  With KV_DECODE_EARLY_INPUTS the split kernel reads
+ *     context_lens, block_tables, the prefix tables and the cache tiles as
+ *     soon as it starts, overlapping the previous kernel's end (q, k_new,
+ *     v_new, the outputs and the workspace still wait for it).  The caller
+ *     guarantees that the kernel launched immediately before this call on
+ *     the stream writes none of those inputs, unless it is a call of this
+ *     library (whose last kernel allows dependent launches only once the
+ *     call's appends are complete).  Inputs written by copies, or by work on
+ *     other streams joined to this one by events, are fine.  It removes ~2 us
+ *     from each step of a decode loop. */
+int paged_decode(void* out, int out_dtype, const void* q, const void* k_new, const void* v_new,
+                 void* k_cache, void* v_cache, int kv_dtype, float k_scale, float v_scale,
+                 int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
+                 const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                 int head_dim, float scale, const int32_t* chunks, const int32_t* seq_chunk,
+                 int num_chunks, unsigned flags, void* workspace, size_t workspace_bytes,
+                 void* stream);
 
 /* ------------------------------------------------------------- diagnostics */
 

@@ -91,8 +91,8 @@ _SIGS = {
     "kv_prefix_chunks": (_i, [_p, _i, _p, _i, _i, _i, _p, _p, ctypes.POINTER(_i)]),
     "paged_decode_prefix_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i,
                                                  ctypes.POINTER(ctypes.c_size_t)]),
-    "paged_decode_prefix": (_i, [_p, _i, _p, _p, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i,
-                                 _i, _i, _f, _p, _p, _i, _p, ctypes.c_size_t, _p]),
+    "paged_decode": (_i, [_p, _i, _p, _p, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i, _i,
+                          _i, _f, _p, _p, _i, ctypes.c_uint, _p, ctypes.c_size_t, _p]),
     "kv_get_device_error": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_i64)]),
     "kv_version": (ctypes.c_char_p, []),
 }
@@ -367,27 +367,35 @@ def alloc_prefix_workspace(num_seqs, num_chunks, num_q_heads, num_kv_heads, head
     return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device or "cuda")
 
 
-def paged_decode_prefix(out, q, k_cache, v_cache, block_tables, context_lens, chunks, seq_chunk,
-                        scale, workspace, k_scale=1.0, v_scale=1.0, k_new=None, v_new=None,
-                        stream=None):
-    """Decode attention with shared prefixes read once per chunk: chunks
-    int32 [nc, 18] and seq_chunk int32 [B] on the device (from
-    prefix_chunks); with k_new/v_new the step's token is appended first (as
-    paged_decode_step).  Other arguments as paged_decode_attention."""
+DECODE_EARLY_INPUTS = 1     # KV_DECODE_EARLY_INPUTS
+
+
+def paged_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, workspace,
+                 k_scale=1.0, v_scale=1.0, k_new=None, v_new=None, chunks=None, seq_chunk=None,
+                 early_inputs=False, stream=None):
+    """One decode step, general form (paged_decode): with k_new/v_new
+    ([B, Hkv, D] bfloat16) the step's token is appended first (as
+    paged_decode_step); with chunks (int32 [nc, 18]) and seq_chunk (int32 [B])
+    on the device (from prefix_chunks) shared prefix blocks are read once per
+    chunk (workspace from alloc_prefix_workspace); early_inputs lets the
+    kernel read the block tables, lengths and caches while the previous
+    kernel on the stream drains (see KV_DECODE_EARLY_INPUTS in the header for
+    the caller's guarantee).  Other arguments as paged_decode_attention."""
     import torch
     B, Hq, D = q.shape
     NB, Hkv, _, _ = k_cache.shape
     out_dtype = F32 if out.dtype == torch.float32 else BF16
-    nc = int(chunks.shape[0])
+    nc = int(chunks.shape[0]) if chunks is not None else 0
     null = ctypes.c_void_p(0)
-    _check(_lib.paged_decode_prefix(
+    _check(_lib.paged_decode(
         _dptr(out), out_dtype, _dptr(q), _dptr(k_new) if k_new is not None else null,
         _dptr(v_new) if v_new is not None else null, _dptr(k_cache), _dptr(v_cache),
         _cache_dtype(k_cache), float(k_scale), float(v_scale), NB, _dptr(block_tables),
         block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D, float(scale),
-        _dptr(chunks) if nc else null, _dptr(seq_chunk) if nc else null, nc, _dptr(workspace),
+        _dptr(chunks) if nc else null, _dptr(seq_chunk) if nc else null, nc,
+        DECODE_EARLY_INPUTS if early_inputs else 0, _dptr(workspace),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
-        "paged_decode_prefix")
+        "paged_decode")
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -423,7 +431,8 @@ class DecodeStepStaging:
     block_tables [B, max_blocks] int32, context_lens [B] int32 -- at 256-byte
     aligned offsets, mirrored by one device buffer, plus an output buffer on
     each side.  A step costs one host-to-device copy, the fused step kernels
-    (paged_decode_step) and one device-to-host copy of the output.  Uploads
+    (paged_decode with the append and KV_DECODE_EARLY_INPUTS) and one
+    device-to-host copy of the output.  Uploads
     and downloads run on two copy streams of their own and the slots
     alternate, so step i+1's upload and step i's download overlap the kernels
     of the steps around them.
@@ -503,8 +512,11 @@ class DecodeStepStaging:
             d.raw.copy_(h.raw, non_blocking=True)
             ev["uploaded"].record(up)
         s.wait_event(ev["uploaded"])
-        paged_decode_step(d.out, d.q, d.k_new, d.v_new, k_cache, v_cache, d.block_tables,
-                          d.context_lens, scale, self.workspace, k_scale, v_scale, stream=s)
+        # the inputs arrive by a copy joined through an event, and the kernel
+        # before is the previous step's: the early reads are safe
+        paged_decode(d.out, d.q, k_cache, v_cache, d.block_tables, d.context_lens, scale,
+                     self.workspace, k_scale, v_scale, k_new=d.k_new, v_new=d.v_new,
+                     early_inputs=True, stream=s)
         ev["computed"].record(s)
         down.wait_event(ev["computed"])
         with torch.cuda.stream(down):

@@ -34,17 +34,19 @@
 //    Both kernels use programmatic dependent launch: each is launched while
 //    the previous kernel on the stream drains and waits on the device
 //    (griddepcontrol.wait) before touching memory, which hides the launch
-//    latency between them.
+//    latency between them.  The merge kernel lets the next kernel start only
+//    after its own wait, so with KV_DECODE_EARLY_INPUTS the next step's
+//    split kernel can read its block tables and cache tiles before waiting.
 //  * Optionally (paged_decode_step) the append of the step's new token is
 //    fused in: the warp that owns a pair's last block writes the new K/V to
 //    the cache and patches its own copy of that tile in shared memory before
 //    using it.
-//  * Shared prefixes (paged_decode_prefix): sequences whose block tables start
-//    with the same blocks ("KV cache complete guide", sections "(3) Prefix
-//    Caching" and "(4) PagedAttention") are cut into chunks whose query rows
-//    fill the whole 16-row MMA tile; each shared tile is read once per chunk,
-//    and the merge kernel adds each member's rows of the chunk's partials to
-//    its own.
+//  * Shared prefixes (paged_decode with a chunk table): sequences whose
+//    block tables start with the same blocks ("KV cache complete guide",
+//    sections "(3) Prefix Caching" and "(4) PagedAttention") are cut into
+//    chunks whose query rows fill the whole 16-row MMA tile; each shared tile
+//    is read once per chunk, and the merge kernel adds each member's rows of
+//    the chunk's partials to its own.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -137,6 +139,7 @@ struct DecodeParams {
     int nc;                      // number of prefix chunks
     int prow;                    // rows per partial slot
     int slot_base;               // first partial slot of the sequence phase
+    int early;                   // read the host-made inputs and caches before the wait
 };
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane)
@@ -805,9 +808,16 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
         prefetch_tmap(&tm_v);
     }
     // let the next kernel on the stream launch now, then wait until the
-    // previous one has finished and its writes are visible
+    // previous one has finished and its writes are visible -- with `early`,
+    // only before the first access to q, k_new, the outputs or the workspace
+    // (the scan, the block-id windows and the first bulk copies overlap the
+    // previous kernel's end)
     pdl_launch_dependents();
-    pdl_wait();
+    bool waited = false;
+    if (!p.early) {
+        pdl_wait();
+        waited = true;
+    }
 
     if (lane == 0) {
 #pragma unroll
@@ -974,6 +984,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
             }
         }
 
+        if (!waited) {
+            pdl_wait();
+            waited = true;
+        }
         // ---- 4. main loop ------------------------------------------------------------
         // Two consecutive tiles of a sequence stream are consumed together
         // where the range allows: one softmax update and one loop turn per 32
@@ -1141,8 +1155,11 @@ template <int D>
 __global__ void __launch_bounds__(kMergeMaxThreads, 4) paged_decode_merge_kernel(const MergeParams p)
 {
     __shared__ float2 sml[kMergeChunk * 8];
-    pdl_launch_dependents();
+    // the next kernel may start only once the split kernel (and with it the
+    // step's appends to the cache) is complete: a following call that reads
+    // its inputs early sees them
     pdl_wait();
+    pdl_launch_dependents();
     const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
     const int t = threadIdx.x;
     const int nthr = blockDim.x;
@@ -1419,7 +1436,8 @@ int check_shape(int num_seqs, int Hq, int Hkv, int D, int kv_dtype)
 
 // Launch with programmatic stream serialisation: the kernel may start while
 // the previous kernel on the stream drains; it waits on the device
-// (griddepcontrol.wait) before touching memory.
+// (griddepcontrol.wait) before touching memory (the split kernel with
+// KV_DECODE_EARLY_INPUTS: before touching what the previous kernel may write).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
                        cudaStream_t st, Args... args)
@@ -1448,6 +1466,7 @@ struct PrefixArgs {
     const int32_t* chunk;
     const int32_t* seq_chunk;
     int nc;
+    unsigned flags;
 };
 
 template <int D, bool FP8>
@@ -1541,6 +1560,7 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.nc = nc;
     dp.prow = nr == 2 ? KV_PREFIX_MAX_ROWS : dp.G;
     dp.slot_base = nr == 2 ? warps_total : 0;
+    dp.early = pre && (pre->flags & KV_DECODE_EARLY_INPUTS) ? 1 : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (ev_begin && cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), st) != cudaSuccess)
@@ -1672,19 +1692,19 @@ extern "C" int paged_decode_prefix_workspace_bytes(int num_seqs, int num_chunks,
     return KV_OK;
 }
 
-extern "C" int paged_decode_prefix(void* out, int out_dtype, const void* q, const void* k_new,
-                                   const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
-                                   float k_scale, float v_scale, int num_blocks,
-                                   const int32_t* block_tables, int max_blocks_per_seq,
-                                   const int32_t* context_lens, int num_seqs, int num_q_heads,
-                                   int num_kv_heads, int head_dim, float scale,
-                                   const int32_t* chunks, const int32_t* seq_chunk,
-                                   int num_chunks, void* workspace, size_t workspace_bytes,
-                                   void* stream)
+extern "C" int paged_decode(void* out, int out_dtype, const void* q, const void* k_new,
+                            const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                            float k_scale, float v_scale, int num_blocks,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, float scale, const int32_t* chunks,
+                            const int32_t* seq_chunk, int num_chunks, unsigned flags,
+                            void* workspace, size_t workspace_bytes, void* stream)
 {
     if ((k_new == nullptr) != (v_new == nullptr)) return KV_ERR_INVALID_ARG;
+    if (flags & ~KV_DECODE_EARLY_INPUTS) return KV_ERR_INVALID_ARG;
     const AppendArgs app = {k_new, v_new, k_cache, v_cache};
-    const PrefixArgs pre = {chunks, seq_chunk, num_chunks};
+    const PrefixArgs pre = {chunks, seq_chunk, num_chunks, flags};
     return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                          num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,

@@ -30,11 +30,12 @@ def half_ulp_bf16(x):
 
 
 def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None, stream=None,
-             fused=False, workspace=None, prefix=None):
+             fused=False, workspace=None, prefix=None, early_inputs=False):
     """Returns (out, k_cache, v_cache) on the device.  fused=False: kv_append
     then paged_decode_attention (two launches); fused=True: paged_decode_step
     (append and attention in one launch).  prefix=(chunks, seq_chunk) (host
-    int32 arrays) runs the shared-prefix entry point instead."""
+    int32 arrays) runs paged_decode with that chunk table instead (early_inputs:
+    with KV_DECODE_EARLY_INPUTS)."""
     import paged_kv_cache_21_gb300 as pk
     NB, Hkv, D = case.num_blocks, case.Hkv, case.D
     cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
@@ -57,17 +58,19 @@ def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None,
         dch = torch.from_numpy(np.ascontiguousarray(chunks, dtype=np.int32)).to(device)
         dsc = torch.from_numpy(np.ascontiguousarray(seq_chunk, dtype=np.int32)).to(device)
         if fused:
-            pk.paged_decode_prefix(out, case.q.to(device), kc, vc, bt, cl, dch, dsc, case.scale,
-                                   ws, case.k_scale, case.v_scale, k_new=case.k_new.to(device),
-                                   v_new=case.v_new.to(device), stream=stream)
+            pk.paged_decode(out, case.q.to(device), kc, vc, bt, cl, case.scale, ws, case.k_scale,
+                            case.v_scale, k_new=case.k_new.to(device),
+                            v_new=case.v_new.to(device), chunks=dch, seq_chunk=dsc,
+                            early_inputs=early_inputs, stream=stream)
         else:
             slots_new = pk.slot_mapping(case.block_tables,
                                         case.context_lens.astype(np.int64) - 1)
             pk.kv_append(case.k_new.to(device), case.v_new.to(device), kc, vc,
                          torch.from_numpy(slots_new).to(device), case.k_scale, case.v_scale,
                          stream=stream)
-            pk.paged_decode_prefix(out, case.q.to(device), kc, vc, bt, cl, dch, dsc, case.scale,
-                                   ws, case.k_scale, case.v_scale, stream=stream)
+            pk.paged_decode(out, case.q.to(device), kc, vc, bt, cl, case.scale, ws, case.k_scale,
+                            case.v_scale, chunks=dch, seq_chunk=dsc, early_inputs=early_inputs,
+                            stream=stream)
         torch.cuda.synchronize()
         return out, kc, vc
     ws = workspace if workspace is not None else pk.alloc_workspace(

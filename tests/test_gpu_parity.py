@@ -509,3 +509,66 @@ def test_token_by_token_decode_equals_causal_prefill(kv_dtype):
         torch.cuda.synchronize()
         err = np.max(np.abs(out.cpu().numpy() - full[:, t]))
         assert err < tol, (t, err)
+
+
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_back_to_back_decode_loop_with_early_inputs(kv_dtype):
+    """The token-by-token decode of two sequences as one stream of launches
+    with no host synchronisation between steps: every step's tables are
+    uploaded before the loop, then paged_decode runs step after step with
+    KV_DECODE_EARLY_INPUTS (each step's kernel reads the block tables and the
+    cache tiles while the previous step drains, and must still see the
+    previous step's append).  Every step equals row t of causal attention,
+    and the outputs equal those of the same loop with the default ordering,
+    bit for bit."""
+    import paged_kv_cache_21_gb300 as pk
+    Hq, Hkv, D, T, NB, MB = 8, 2, 128, 90, 16, 8
+    g = torch.Generator().manual_seed(191 + kv_dtype)
+    Q = torch.randn((2, T, Hq, D), generator=g).to(torch.bfloat16)
+    Kt = torch.randn((2, T, Hkv, D), generator=g).to(torch.bfloat16)
+    Vt = torch.randn((2, T, Hkv, D), generator=g).to(torch.bfloat16)
+    ks = vs = 1.0
+    if kv_dtype == workloads.FP8_E4M3:
+        ks = float(np.float32(float(Kt.abs().max())) / np.float32(448.0))
+        vs = float(np.float32(float(Vt.abs().max())) / np.float32(448.0))
+    alloc = pk.BlockAllocator(NB, Hkv, D, kv_dtype)
+    alloc.add(0, 0)
+    alloc.add(1, 0)
+    tables, lens = [], []
+    for t in range(T):
+        _, bt, ln, (cs, _cd) = alloc.step([0, 1], MB)
+        assert len(cs) == 0
+        tables.append(bt.copy())
+        lens.append(ln.copy())
+    d_bt = torch.from_numpy(np.stack(tables)).cuda()          # [T, 2, MB]
+    d_len = torch.from_numpy(np.stack(lens)).cuda()           # [T, 2]
+    d_q = Q.transpose(0, 1).contiguous().cuda()               # [T, 2, Hq, D]
+    d_k = Kt.transpose(0, 1).contiguous().cuda()
+    d_v = Vt.transpose(0, 1).contiguous().cuda()
+    cdt = torch.bfloat16 if kv_dtype == workloads.BF16 else torch.uint8
+    ws = pk.alloc_workspace(2, Hq, Hkv, D, kv_dtype)
+    outs = {}
+    for early in (False, True):
+        kc = torch.zeros((NB, Hkv, 16, D), dtype=cdt, device="cuda")
+        vc = torch.zeros_like(kc)
+        out = torch.empty((T, 2, Hq, D), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        for t in range(T):
+            pk.paged_decode(out[t], d_q[t], kc, vc, d_bt[t], d_len[t], 1 / math.sqrt(D), ws, ks,
+                            vs, k_new=d_k[t], v_new=d_v[t], early_inputs=early)
+        torch.cuda.synchronize()
+        outs[early] = out.cpu()
+    assert torch.equal(outs[False], outs[True])
+    if kv_dtype == workloads.FP8_E4M3:
+        Kv = oracle.e4m3_decode_array(oracle.quantize_e4m3(bf16_bits(Kt), ks)) * ks
+        Vv = oracle.e4m3_decode_array(oracle.quantize_e4m3(bf16_bits(Vt), vs)) * vs
+    else:
+        Kv, Vv = oracle.bf16_bits_to_f64(bf16_bits(Kt)), oracle.bf16_bits_to_f64(bf16_bits(Vt))
+    Qv = oracle.bf16_bits_to_f64(bf16_bits(Q))
+    tol = H.tolerance(kv_dtype)
+    for s in range(2):
+        for h in range(Hq):
+            ref = oracle.causal_attention(Qv[s, :, h], Kv[s, :, h // (Hq // Hkv)],
+                                          Vv[s, :, h // (Hq // Hkv)], 1 / math.sqrt(D))
+            err = np.max(np.abs(outs[True][:, s, h].numpy() - ref))
+            assert err < tol, (s, h, err)

@@ -1,4 +1,4 @@
-"""Shared-prefix decoding on the GPU (paged_decode_prefix) against the CPU
+"""Shared-prefix decoding on the GPU (paged_decode with a chunk table) against the CPU
 oracle.  The result is plain decode attention ("KV Cache" (heepie.pages.dev),
 section "Self-Attention") whatever the chunking: the oracle attends each
 sequence over its own block-table row; the kernel reads the shared blocks
@@ -33,9 +33,11 @@ def chunks_of(case, min_blocks=1):
                             min_blocks=min_blocks)
 
 
-def check_prefix(case, fused, out_dtype=torch.bfloat16, pair_select=None, what="", prefix=None):
+def check_prefix(case, fused, out_dtype=torch.bfloat16, pair_select=None, what="", prefix=None,
+                 early_inputs=False):
     prefix = prefix if prefix is not None else chunks_of(case)
-    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype, fused=fused, prefix=prefix)
+    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype, fused=fused, prefix=prefix,
+                             early_inputs=early_inputs)
     okc, ovc = H.oracle_caches(case)
     assert np.array_equal(cache_bits(kc), okc), "K cache differs " + what
     assert np.array_equal(cache_bits(vc), ovc), "V cache differs " + what
@@ -51,10 +53,12 @@ def shared_case(Hq, Hkv, D=128, B=24, group=8, kv_dtype=workloads.BF16, n_hi=300
     return workloads.make_case("3", override=ov, seed=seed)
 
 
-@pytest.mark.parametrize("fused", [False, True], ids=["append+attend", "fused_step"])
-def test_config3_shape_full_compare(fused):
+@pytest.mark.parametrize("fused,early", [(False, False), (True, False), (True, True)],
+                         ids=["append+attend", "fused_step", "fused_step_early_inputs"])
+def test_config3_shape_full_compare(fused, early):
     case = workloads.make_case("3", override={"B": 32})
-    err, nc, _ = check_prefix(case, fused, what="config 3 B=32 fused=%s" % fused)
+    err, nc, _ = check_prefix(case, fused, what="config 3 B=32 fused=%s" % fused,
+                              early_inputs=early)
     assert nc > 0
     print("config 3 B=32 prefix fused=%s: %d chunks, max abs err %.3g" % (fused, nc, err))
 
@@ -121,9 +125,9 @@ def test_deterministic_and_block_relabelling_invariant():
     outs = []
     for _ in range(2):
         o = torch.empty_like(out1)
-        pk.paged_decode_prefix(o, case.q.cuda(), kc2, vc2, torch.from_numpy(bt2).cuda(),
-                               torch.from_numpy(case.context_lens).cuda(), dch, dsc,
-                               case.scale, ws)
+        pk.paged_decode(o, case.q.cuda(), kc2, vc2, torch.from_numpy(bt2).cuda(),
+                        torch.from_numpy(case.context_lens).cuda(), case.scale, ws,
+                        chunks=dch, seq_chunk=dsc)
         outs.append(o)
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), outs[0].view(torch.int16))
