@@ -6,7 +6,8 @@
  * i.e. the new token's K/V is appended to the cache first and the new query
  * then attends over the whole cache, including itself ("Transformer
  * attention mask and KV cache inference", section "Prefill and decode
- * phases").
+ * phases").  paged_decode_step does the two GPU parts in one launch pair;
+ * paged_decode is its general form (shared-prefix chunks, early inputs).
  *
  * Conventions shared by every entry point
  *   - Every function returns an int status: KV_OK (0) or a negative KV_ERR_*.
