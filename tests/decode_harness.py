@@ -34,8 +34,9 @@ def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None,
     """Returns (out, k_cache, v_cache) on the device.  fused=False: kv_append
     then paged_decode_attention (two launches); fused=True: paged_decode_step
     (append and attention in one launch).  prefix=(chunks, seq_chunk) (host
-    int32 arrays) runs paged_decode with that chunk table instead (early_inputs:
-    with KV_DECODE_EARLY_INPUTS)."""
+    int32 arrays) runs paged_decode with that chunk table instead.  early_inputs:
+    paged_decode with KV_DECODE_EARLY_INPUTS (with fused=True and no prefix,
+    the call bench.py times)."""
     import paged_kv_cache_21_gb300 as pk
     NB, Hkv, D = case.num_blocks, case.Hkv, case.D
     cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
@@ -75,7 +76,12 @@ def gpu_step(case, out_dtype=torch.bfloat16, device="cuda", pool_overrides=None,
         return out, kc, vc
     ws = workspace if workspace is not None else pk.alloc_workspace(
         case.B, case.Hq, Hkv, D, case.kv_dtype, device=device)
-    if fused:
+    if fused and early_inputs:
+        # the benchmark's call: fused append, early reads of tables and caches
+        pk.paged_decode(out, case.q.to(device), kc, vc, bt, cl, case.scale, ws, case.k_scale,
+                        case.v_scale, k_new=case.k_new.to(device), v_new=case.v_new.to(device),
+                        early_inputs=True, stream=stream)
+    elif fused:
         pk.paged_decode_step(out, case.q.to(device), case.k_new.to(device),
                              case.v_new.to(device), kc, vc, bt, cl, case.scale, ws,
                              case.k_scale, case.v_scale, stream=stream)

@@ -36,8 +36,9 @@ def cache_bits(t):
     return t.numpy()
 
 
-def check_case(case, out_dtype=torch.bfloat16, pair_select=None, what="", fused=False):
-    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype, fused=fused)
+def check_case(case, out_dtype=torch.bfloat16, pair_select=None, what="", fused=False,
+               early_inputs=False):
+    out, kc, vc = H.gpu_step(case, out_dtype=out_dtype, fused=fused, early_inputs=early_inputs)
     okc, ovc = H.oracle_caches(case)
     assert np.array_equal(cache_bits(kc), okc), "K cache differs from oracle " + what
     assert np.array_equal(cache_bits(vc), ovc), "V cache differs from oracle " + what
@@ -108,7 +109,8 @@ def test_copy_blocks_copies_whole_blocks():
 
 # ------------------------------------------------------------- configs
 
-@pytest.mark.parametrize("fused", [False, True], ids=["append+attend", "fused_step"])
+@pytest.mark.parametrize("fused,early", [(False, False), (True, False), (True, True)],
+                         ids=["append+attend", "fused_step", "fused_early_inputs"])
 @pytest.mark.parametrize("cfg,override", [
     ("1", None),
     ("2", {"B": 3}),                       # 3 x 8193 tokens: many splits + ragged tail
@@ -117,20 +119,23 @@ def test_copy_blocks_copies_whole_blocks():
     ("5a", {"B": 3}),                      # E4M3 cache
     ("5b", {"B": 2}),                      # MHA, G = 1
 ])
-def test_config_shapes_full_compare(cfg, override, fused):
+def test_config_shapes_full_compare(cfg, override, fused, early):
     case = workloads.make_case(cfg, override=override)
-    err = check_case(case, what="config %s %s" % (cfg, override), fused=fused)
-    print("config %s %s fused=%s: max abs err %.3g" % (cfg, override, fused, err))
+    err = check_case(case, what="config %s %s" % (cfg, override), fused=fused,
+                     early_inputs=early)
+    print("config %s %s fused=%s early=%s: max abs err %.3g" % (cfg, override, fused, early,
+                                                                 err))
 
 
 @pytest.mark.parametrize("cfg,nsample", [("2", 24), ("3", 24), ("4", 8), ("5a", 24), ("5b", 24)])
 def test_config_full_size_sampled(cfg, nsample):
-    """Full-size configuration in the benchmark's launch configuration (the
-    fused step); the oracle computes a seeded sample of (sequence, KV head)
-    pairs, the caches are compared in full."""
+    """Full-size configuration through the call the benchmark times
+    (paged_decode: fused append, early inputs); the oracle computes a seeded
+    sample of (sequence, KV head) pairs, the caches are compared in full."""
     case = workloads.make_case(cfg)
     sel = H.sample_pairs(case, nsample, seed=int(cfg[0]))
-    err = check_case(case, pair_select=sel, what="config %s full size" % cfg, fused=True)
+    err = check_case(case, pair_select=sel, what="config %s full size" % cfg, fused=True,
+                     early_inputs=True)
     print("config %s full size: max abs err %.3g over %d pairs" % (cfg, err, int(sel.sum())))
 
 
