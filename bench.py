@@ -527,6 +527,38 @@ def run_ours(args):
         e2e = {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": stg.h2d_bytes,
                "d2h_bytes_per_step": stg.d2h_bytes}
+        del stg
+
+        # the same with the kernels reading the pinned host slots in place
+        # (no copies: NVLink-C2C on a Grace-Blackwell node)
+        zc = pk.DecodeStepStaging(B, Hq, Hkv, D, case.max_blocks, case.kv_dtype, device=device,
+                                  zero_copy=True)
+        for j in range(2):
+            hs = zc.host(j)
+            hs.q.copy_(q.cpu())
+            hs.k_new.copy_(k_new.cpu())
+            hs.v_new.copy_(v_new.cpu())
+            hs.block_tables.copy_(torch.from_numpy(case.block_tables))
+            hs.context_lens.copy_(torch.from_numpy(case.context_lens))
+        zcount = [0]
+
+        def zc_step(_e=None):
+            zc.step(zcount[0], kc, vc, case.scale, case.k_scale, case.v_scale, stream=stream)
+            zcount[0] += 1
+
+        for _ in range(max(args.warmup, 3)):
+            zc_step()
+        torch.cuda.synchronize()
+        zc_ms = reduce_max(timed(K, zc_step, 0)[0], world, device)
+        torch.cuda.synchronize()
+        assert torch.equal(zc.host(zcount[0] - 1).out.view(torch.int16),
+                           out.cpu().view(torch.int16))
+        e2e["zero_copy"] = {"value": total_bytes / (zc_ms * 1e-3) / 1e9, "unit": "GB/s",
+                            "ms_per_step": zc_ms, "h2d_bytes_per_step": zc.h2d_bytes,
+                            "d2h_bytes_per_step": zc.d2h_bytes,
+                            "how": "inputs read and output written in pinned host memory "
+                                   "by the kernels (NVLink-C2C), no copies"}
+        del zc
 
     # same-run copy ceiling: a plain device-to-device copy of 1 GiB (read + write bytes)
     src = torch.ones(1 << 29, dtype=torch.int16, device=device)

@@ -14,7 +14,13 @@
  *     Nothing throws across this boundary.
  *   - Device buffers are plain device pointers owned by the caller; the
  *     library never allocates, frees or retains device memory.  Host
- *     buffers are plain host pointers, also caller-owned.
+ *     buffers are plain host pointers, also caller-owned.  The per-step
+ *     buffers of the decode entry points (q, k_new, v_new, block_tables,
+ *     context_lens, prefix tables, out) may also be pinned host memory that
+ *     the device can address (cudaHostAlloc / cudaHostRegister with unified
+ *     addressing): the kernels then read and write them in place, over the
+ *     coherent NVLink-C2C link of a Grace-Blackwell node, with no copy.  The
+ *     caches and the workspace must be device memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  GPU entry points only enqueue work and return; a launch
  *     failure is reported as KV_ERR_CUDA.  Faults found by the kernels'

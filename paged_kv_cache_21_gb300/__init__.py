@@ -437,6 +437,11 @@ class DecodeStepStaging:
     alternate, so step i+1's upload and step i's download overlap the kernels
     of the steps around them.
 
+    With ``zero_copy=True`` there are no copies and no device slots: the
+    kernels read the step's inputs from the pinned host slot and write the
+    output into it directly (over NVLink-C2C on a Grace-Blackwell node), and
+    the stream of steps stays one chain of kernel launches.
+
     Use: fill ``host(i)`` views of slot i % slots (``q``, ``k_new``,
     ``v_new``, ``block_tables``, ``context_lens``) once ``ready_for_input(i)``
     holds, call ``step(i, ...)``, and read ``host(i).out`` after
@@ -448,9 +453,10 @@ class DecodeStepStaging:
         pass
 
     def __init__(self, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks,
-                 kv_dtype=BF16, device=None, out_dtype=None, slots=2):
+                 kv_dtype=BF16, device=None, out_dtype=None, slots=2, zero_copy=False):
         import torch
         self.device = torch.device(device or "cuda")
+        self.zero_copy = bool(zero_copy)
         B, Hq, Hkv, D = num_seqs, num_q_heads, num_kv_heads, head_dim
         parts = [("q", (B, Hq, D), torch.bfloat16), ("k_new", (B, Hkv, D), torch.bfloat16),
                  ("v_new", (B, Hkv, D), torch.bfloat16),
@@ -467,12 +473,16 @@ class DecodeStepStaging:
         for _ in range(slots):
             h, d = self._Slot(), self._Slot()
             h.raw = torch.empty(off, dtype=torch.uint8).pin_memory()
-            d.raw = torch.empty(off, dtype=torch.uint8, device=self.device)
+            h.out = torch.empty((B, Hq, D), dtype=od).pin_memory()
+            if self.zero_copy:
+                d = h                   # the kernels address the pinned slot itself
+            else:
+                d.raw = torch.empty(off, dtype=torch.uint8, device=self.device)
+                d.out = torch.empty((B, Hq, D), dtype=od, device=self.device)
             for name, (o, shape, dt, nb) in offs.items():
                 setattr(h, name, h.raw[o:o + nb].view(dt).view(shape))
-                setattr(d, name, d.raw[o:o + nb].view(dt).view(shape))
-            h.out = torch.empty((B, Hq, D), dtype=od).pin_memory()
-            d.out = torch.empty((B, Hq, D), dtype=od, device=self.device)
+                if d is not h:
+                    setattr(d, name, d.raw[o:o + nb].view(dt).view(shape))
             ev = {k: torch.cuda.Event() for k in ("uploaded", "computed", "downloaded")}
             self._slots.append((h, d, ev))
         self.upload_stream = torch.cuda.Stream(self.device)
@@ -484,6 +494,8 @@ class DecodeStepStaging:
 
     @property
     def h2d_bytes(self):
+        """Bytes of inputs a step moves host to device (copied, or read in
+        place with zero_copy)."""
         return self.nbytes
 
     @property
@@ -493,11 +505,13 @@ class DecodeStepStaging:
 
     def ready_for_input(self, i):
         """Block the host until slot i % slots may be refilled (its previous
-        upload has finished)."""
-        self._slots[i % len(self._slots)][2]["uploaded"].synchronize()
+        upload has finished; with zero_copy, its previous step)."""
+        ev = self._slots[i % len(self._slots)][2]
+        (ev["computed"] if self.zero_copy else ev["uploaded"]).synchronize()
 
     def wait_output(self, i):
-        self._slots[i % len(self._slots)][2]["downloaded"].synchronize()
+        ev = self._slots[i % len(self._slots)][2]
+        (ev["computed"] if self.zero_copy else ev["downloaded"]).synchronize()
 
     def step(self, i, k_cache, v_cache, scale, k_scale=1.0, v_scale=1.0, stream=None):
         """Upload slot i's inputs, run the fused decode step on `stream`,
@@ -505,6 +519,14 @@ class DecodeStepStaging:
         import torch
         h, d, ev = self._slots[i % len(self._slots)]
         s = stream or torch.cuda.current_stream(self.device)
+        if self.zero_copy:
+            # the slot is refilled by the host only after ready_for_input(i),
+            # and the kernel before is the previous step's: early reads are safe
+            paged_decode(h.out, h.q, k_cache, v_cache, h.block_tables, h.context_lens, scale,
+                         self.workspace, k_scale, v_scale, k_new=h.k_new, v_new=h.v_new,
+                         early_inputs=True, stream=s)
+            ev["computed"].record(s)
+            return
         up, down = self.upload_stream, self.download_stream
         # the device slot is free once its previous step has been computed
         up.wait_event(ev["computed"])

@@ -577,3 +577,31 @@ def test_back_to_back_decode_loop_with_early_inputs(kv_dtype):
                                           Vv[s, :, h // (Hq // Hkv)], 1 / math.sqrt(D))
             err = np.max(np.abs(outs[True][:, s, h].numpy() - ref))
             assert err < tol, (s, h, err)
+
+
+def test_pinned_host_buffers_read_in_place():
+    """The per-step buffers (q, k_new, v_new, block tables, lengths, out) in
+    pinned host memory: the kernels read and write them in place, and the
+    result equals the device-buffer call bit for bit (caches identical too);
+    the zero-copy staging mode runs the same steps."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(6, 32, 8, 128, [1, 40, 700, 3000, 9000, 16], seed=61)
+    out_d, kc_d, vc_d = H.gpu_step(case, fused=True, early_inputs=True)
+    NB = case.num_blocks
+    kc = torch.zeros((NB, case.Hkv, 16, case.D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    pk.kv_append(case.pool_k.cuda(), case.pool_v.cuda(), kc, vc,
+                 torch.arange(NB * 16, dtype=torch.int64, device="cuda"))
+    stg = pk.DecodeStepStaging(case.B, case.Hq, case.Hkv, case.D, case.max_blocks,
+                               zero_copy=True)
+    hs = stg.host(0)
+    hs.q.copy_(case.q)
+    hs.k_new.copy_(case.k_new)
+    hs.v_new.copy_(case.v_new)
+    hs.block_tables.copy_(torch.from_numpy(case.block_tables))
+    hs.context_lens.copy_(torch.from_numpy(case.context_lens))
+    stg.step(0, kc, vc, case.scale)
+    stg.wait_output(0)
+    assert torch.equal(hs.out.view(torch.int16), out_d.cpu().view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc_d.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc_d.view(torch.int16))
