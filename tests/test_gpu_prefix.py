@@ -191,3 +191,64 @@ def test_long_shared_prompt(override, nsample):
     err, nc, _ = check_prefix(case, True, pair_select=sel, what="3L %s" % override)
     assert nc > 0
     print("3L %s: %d chunks, max abs err %.3g" % (override, nc, err))
+
+
+def test_forked_prompt_through_allocator_chunks_and_kernel():
+    """A shared system prompt the way a server holds one: a 200-token prompt
+    prefilled once, forked to 8 sequences (blocks shared by reference count),
+    then 12 decode steps.  Each step: kv_step plans the appends (copy-on-write
+    of the shared partial tail block on the first step), kv_prefix_chunks
+    finds the shared blocks in the live block tables, and paged_decode
+    appends and attends with the chunk table; the oracle replays the same
+    tables on its own cache copy."""
+    import math
+    import paged_kv_cache_21_gb300 as pk
+    from workloads import bf16_bits
+    import oracle
+    Hq, Hkv, D, NB, MB, P0 = 32, 8, 128, 256, 16, 200
+    alloc = pk.BlockAllocator(NB, Hkv, D)
+    g = torch.Generator().manual_seed(57)
+    kc = torch.zeros((NB, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    okc = np.zeros((NB, Hkv, 16, D), dtype=np.uint16)
+    ovc = np.zeros_like(okc)
+    alloc.add(100, P0)
+    _, row = alloc.info(100)
+    pk_ = torch.randn((P0, Hkv, D), generator=g).to(torch.bfloat16)
+    pv_ = torch.randn((P0, Hkv, D), generator=g).to(torch.bfloat16)
+    slots0 = np.array([row[p // 16] * 16 + p % 16 for p in range(P0)], dtype=np.int64)
+    pk.kv_append(pk_.cuda(), pv_.cuda(), kc, vc, torch.from_numpy(slots0).cuda())
+    oracle.append(okc, ovc, bf16_bits(pk_), bf16_bits(pv_), slots0, oracle.BF16)
+    ids = list(range(8))
+    for sid in ids:
+        alloc.fork(100, sid, P0)
+    alloc.free(100)
+    ws = pk.alloc_prefix_workspace(len(ids), len(ids) // 2, Hq, Hkv, D)
+    scale = 1 / math.sqrt(D)
+    for step in range(12):
+        slots, bt, lens, (cs, cd) = alloc.step(ids, MB)
+        if len(cs):
+            pk.kv_copy_blocks(kc, vc, torch.from_numpy(cs).cuda(), torch.from_numpy(cd).cuda())
+            for s_, d_ in zip(cs, cd):
+                okc[d_] = okc[s_]
+                ovc[d_] = ovc[s_]
+        chunks, seq_chunk = pk.prefix_chunks(bt, lens, Hq // Hkv)
+        # 200 tokens = 12 full blocks shared by all 8 (the 13th is each one's own copy)
+        assert len(chunks) == 2 and all(int(r[0]) >= 12 for r in chunks)
+        q = torch.randn((len(ids), Hq, D), generator=g).to(torch.bfloat16)
+        k = torch.randn((len(ids), Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((len(ids), Hkv, D), generator=g).to(torch.bfloat16)
+        out = torch.empty((len(ids), Hq, D), dtype=torch.float32, device="cuda")
+        pk.paged_decode(out, q.cuda(), kc, vc, torch.from_numpy(bt).cuda(),
+                        torch.from_numpy(lens).cuda(), scale, ws, k_new=k.cuda(), v_new=v.cuda(),
+                        chunks=torch.from_numpy(chunks).cuda(),
+                        seq_chunk=torch.from_numpy(seq_chunk).cuda(), early_inputs=True)
+        oracle.append(okc, ovc, bf16_bits(k), bf16_bits(v), slots, oracle.BF16)
+        ref = oracle.paged_attention(oracle.bf16_bits_to_f64(bf16_bits(q)), okc, ovc, bt, lens,
+                                     scale)
+        torch.cuda.synchronize()
+        assert np.array_equal(kc.cpu().view(torch.int16).numpy().view(np.uint16), okc), step
+        assert np.max(np.abs(out.cpu().numpy() - ref)) < H.tolerance(workloads.BF16), step
+    for sid in ids:
+        alloc.free(sid)
+    assert alloc.stats()[0] == NB
