@@ -252,3 +252,41 @@ def test_forked_prompt_through_allocator_chunks_and_kernel():
     for sid in ids:
         alloc.free(sid)
     assert alloc.stats()[0] == NB
+
+
+def test_general_step_replays_in_a_cuda_graph():
+    """paged_decode with a chunk table and early inputs, captured in a CUDA
+    graph (programmatic edges inside the graph) and replayed: every replay
+    equals the eager call bit for bit (the append rewrites the same token)."""
+    import paged_kv_cache_21_gb300 as pk
+    case = shared_case(32, 8, B=16, seed=23)
+    chunks, seq_chunk = chunks_of(case)
+    out_ref, kc, vc = H.gpu_step(case, fused=True, prefix=(chunks, seq_chunk),
+                                 early_inputs=True)
+    q = case.q.cuda()
+    kn, vn = case.k_new.cuda(), case.v_new.cuda()
+    bt = torch.from_numpy(case.block_tables).cuda()
+    cl = torch.from_numpy(case.context_lens).cuda()
+    dch, dsc = torch.from_numpy(chunks).cuda(), torch.from_numpy(seq_chunk).cuda()
+    ws = pk.alloc_prefix_workspace(case.B, len(chunks), case.Hq, case.Hkv, case.D)
+    out = torch.empty_like(out_ref)
+
+    def call(stream):
+        pk.paged_decode(out, q, kc, vc, bt, cl, case.scale, ws, k_new=kn, v_new=vn,
+                        chunks=dch, seq_chunk=dsc, early_inputs=True, stream=stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call(s)
+        call(s)                      # two steps: a programmatic edge inside the graph
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out_ref.view(torch.int16))
