@@ -25,7 +25,9 @@
 //    then P (the running-softmax weights, kept in registers; for bf16 split
 //    into a bf16 high and low part so they carry ~16 bits) times V.  The C
 //    fragment of the score MMA is exactly the B fragment of the PV MMA, so
-//    scores never leave registers.
+//    scores never leave registers.  Two consecutive tiles of a pair are
+//    consumed together where the range allows: one online-softmax update per
+//    32 tokens.
 //  * Warps whose range covers a whole (sequence, KV head) write the output
 //    directly; the others store an unnormalised partial output with its
 //    (max, sum) -- plain stores, no atomics or fences, so the split kernel
@@ -1480,7 +1482,7 @@ cudaError_t launch_split(int nr, unsigned grid, cudaStream_t st, const CUtensorM
                       st, mk, mv, dp);
 }
 
-// Validate, build the tensor maps and launch the decode kernel (one launch).
+// Validate, build the tensor maps and launch the split and merge kernels.
 int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
                   const void* v_cache, int kv_dtype, float k_scale, float v_scale, int num_blocks,
                   const int32_t* block_tables, int max_blocks_per_seq,
