@@ -167,6 +167,47 @@ int kv_seq_info(kv_alloc_t* a, int64_t seq_id, int64_t* len, int32_t* row, int m
 int kv_alloc_stats(kv_alloc_t* a, int* free_blocks, int* used_blocks, int* num_seqs,
                    int block, int* refcount);
 
+/* The allocator's shape: pool blocks, KV heads, head dim and cache dtype, so
+ * that a trace can state the per-layer cache shape
+ * [num_blocks][num_kv_heads][16][head_dim].  Any pointer may be NULL. */
+int kv_alloc_shape(kv_alloc_t* a, int* num_blocks, int* num_kv_heads, int* head_dim,
+                   int* kv_dtype);
+
+/* Debug trace of the cache state: the fields that "Transformer attention mask
+ * and KV cache inference", section "Implementation and verification
+ * procedure", wants a trace to keep, so that a wrong output can be narrowed
+ * down to a broken state contract.  One row
+ * of KV_TRACE_FIELDS int64 per sequence, fields indexed by KV_TRACE_*:
+ *   SEQ_ID         the request id;
+ *   SLOT           its batch row in the last kv_step or kv_seq_reorder that
+ *                  named it (-1: none yet);
+ *   LEN            current length (tokens held);
+ *   POSITION       position offset the next appended token takes (equal to
+ *                  LEN: a paged sequence holds no padding);
+ *   BLOCKS         blocks held;
+ *   SHARED_BLOCKS  of those, blocks whose reference count is above 1;
+ *   CACHE_BYTES    K + V bytes of the held blocks for one layer
+ *                  (BLOCKS * 2 * 16 * num_kv_heads * head_dim * element size);
+ *   REORDER_SRC    the src_index its row had in the last kv_seq_reorder that
+ *                  named it, i.e. the reorder permutation (-1: never).
+ * A decode step has no mask tensor: each row attends to LEN keys (mask shape
+ * [1, LEN]).  seq_ids != NULL: rows for those n sequences in that order
+ * (KV_ERR_NOT_FOUND for an unknown id).  seq_ids == NULL: every live
+ * sequence in ascending id order; n is the capacity of rows in sequences and
+ * KV_ERR_INVALID_ARG if fewer than the live count.  rows is a host array of
+ * [n][KV_TRACE_FIELDS] int64; *count (may be NULL) gets the rows written.
+ * Reads only; nothing changes. */
+#define KV_TRACE_FIELDS 8
+#define KV_TRACE_SEQ_ID 0
+#define KV_TRACE_SLOT 1
+#define KV_TRACE_LEN 2
+#define KV_TRACE_POSITION 3
+#define KV_TRACE_BLOCKS 4
+#define KV_TRACE_SHARED_BLOCKS 5
+#define KV_TRACE_CACHE_BYTES 6
+#define KV_TRACE_REORDER_SRC 7
+int kv_alloc_trace(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* rows, int* count);
+
 /* Slot of position positions[i] of sequence row i of block_tables (host):
  *     slot = block_tables[i][pos / 16] * 16 + pos % 16
  * ("KV Cache, Flash Attention and inference optimization", section
@@ -239,7 +280,11 @@ int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads
  * kernel merges with the log-sum-exp rule ("KV Cache, Flash Attention and
  * inference optimization", section "Numerical trick": the running (max, sum)
  * makes the tiled result exact).  A sequence with context_lens[s] == 0 gets
- * zeros.  Both kernels use programmatic dependent launch: each may start
+ * zeros.  Bad table entries never fault: a block id outside [0, num_blocks)
+ * is not read (its sequence's output is then unspecified) and a context
+ * length outside [0, 16*max_blocks_per_seq] is clamped into that range; each
+ * raises its KV_DEVERR_* flag (kv_get_device_error, the first bad value as
+ * the detail).  Both kernels use programmatic dependent launch: each may start
  * while the previous kernel on the stream drains, and waits on the device for
  * it to finish before reading or writing any buffer.  Deterministic: the same
  * inputs on the same device give bit-identical outputs, whatever the physical

@@ -41,6 +41,11 @@ DEVERR_CONTEXT_TOO_LONG = 4
 DEVERR_PIPELINE_TIMEOUT = 8
 DEVERR_BAD_PREFIX = 16
 
+# columns of a kv_alloc_trace row (KV_TRACE_*)
+TRACE_KEYS = ("seq_id", "slot", "len", "position", "blocks", "shared_blocks", "cache_bytes",
+              "reorder_src")
+TRACE_FIELDS = len(TRACE_KEYS)
+
 _ERRNAMES = {KV_ERR_INVALID_ARG: "KV_ERR_INVALID_ARG", KV_ERR_OUT_OF_BLOCKS: "KV_ERR_OUT_OF_BLOCKS",
              KV_ERR_UNSUPPORTED: "KV_ERR_UNSUPPORTED", KV_ERR_CUDA: "KV_ERR_CUDA",
              KV_ERR_NOT_FOUND: "KV_ERR_NOT_FOUND", KV_ERR_EXISTS: "KV_ERR_EXISTS",
@@ -76,6 +81,9 @@ _SIGS = {
     "kv_seq_info": (_i, [_p, _i64, ctypes.POINTER(_i64), _p, _i, ctypes.POINTER(_i)]),
     "kv_alloc_stats": (_i, [_p, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i), _i,
                             ctypes.POINTER(_i)]),
+    "kv_alloc_shape": (_i, [_p, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i),
+                            ctypes.POINTER(_i)]),
+    "kv_alloc_trace": (_i, [_p, _p, _i, _p, ctypes.POINTER(_i)]),
     "kv_slot_mapping": (_i, [_p, _i, _p, _i, _p]),
     "kv_append": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _f, _f, _p]),
     "kv_copy_blocks": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p]),
@@ -237,6 +245,47 @@ class BlockAllocator:
         _check(_lib.kv_alloc_stats(self._h, ctypes.byref(fb), ctypes.byref(ub), ctypes.byref(ns),
                                    block, ctypes.byref(rc)), "kv_alloc_stats")
         return fb.value, ub.value, ns.value, (rc.value if block >= 0 else None)
+
+    def shape(self):
+        """Per-layer cache shape [num_blocks, num_kv_heads, 16, head_dim] and dtype."""
+        nb, h, d, dt = _i(0), _i(0), _i(0), _i(0)
+        _check(_lib.kv_alloc_shape(self._h, ctypes.byref(nb), ctypes.byref(h), ctypes.byref(d),
+                                   ctypes.byref(dt)), "kv_alloc_shape")
+        return (nb.value, h.value, BLOCK_SIZE, d.value), dt.value
+
+    def trace(self, seq_ids=None):
+        """Debug trace of the cache state, one dict per sequence (the given
+        ids in order, else every live sequence by ascending id): request id,
+        batch slot, length, position offset, blocks, shared blocks, cache
+        bytes per layer, the last reorder's source row, and the decode mask
+        shape [1, length]."""
+        if seq_ids is None:
+            n = self.stats()[2]
+            ids_ptr = None
+        else:
+            ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+            n = ids.shape[0]
+            ids_ptr = _np_ptr(ids)
+        rows = np.empty((max(n, 1), TRACE_FIELDS), dtype=np.int64)
+        cnt = _i(0)
+        _check(_lib.kv_alloc_trace(self._h, ids_ptr, n, _np_ptr(rows), ctypes.byref(cnt)),
+               "kv_alloc_trace")
+        out = []
+        for r in rows[:cnt.value]:
+            rec = dict(zip(TRACE_KEYS, (int(x) for x in r)))
+            rec["mask_shape"] = [1, rec["len"]]
+            out.append(rec)
+        return out
+
+    def dump(self, seq_ids=None):
+        """The trace as text: a header line with the pool and cache shape,
+        then one JSON line per sequence."""
+        import json
+        shape, dt = self.shape()
+        fb, ub, ns, _ = self.stats()
+        head = {"kv_shape": list(shape), "kv_dtype": "fp8_e4m3" if dt == FP8_E4M3 else "bf16",
+                "free_blocks": fb, "used_blocks": ub, "num_seqs": ns}
+        return "\n".join([json.dumps(head)] + [json.dumps(r) for r in self.trace(seq_ids)])
 
 
 # -------------------------------------------------------------------- GPU ops

@@ -25,6 +25,8 @@ namespace {
 struct Seq {
     int64_t len = 0;
     std::vector<int32_t> blocks;
+    int32_t slot = -1;         // row in the last kv_step / kv_seq_reorder naming it
+    int32_t reorder_src = -1;  // src_index of that row in the last kv_seq_reorder
 };
 
 int64_t ceil_blocks(int64_t len) { return (len + KV_BLOCK_SIZE - 1) / KV_BLOCK_SIZE; }
@@ -187,6 +189,7 @@ int kv_step(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* slot_mapping,
         }
         slot_mapping[i] = (int64_t)s.blocks[bi] * KV_BLOCK_SIZE + pos % KV_BLOCK_SIZE;
         s.len = pos + 1;
+        s.slot = i;
         context_lens[i] = (int32_t)s.len;
         int32_t* row = block_tables + (int64_t)i * max_blocks;
         int nb = (int)s.blocks.size();
@@ -219,7 +222,11 @@ int kv_seq_reorder(kv_alloc_t* a, const int64_t* seq_ids, const int32_t* src_ind
         for (int32_t b : old[src_index[i]].blocks) a->refcount[b] += 1;
     for (int i = 0; i < n; ++i)
         for (int32_t b : old[i].blocks) a->release(b);
-    for (int i = 0; i < n; ++i) *rows[i] = old[src_index[i]];
+    for (int i = 0; i < n; ++i) {
+        *rows[i] = old[src_index[i]];
+        rows[i]->slot = i;
+        rows[i]->reorder_src = src_index[i];
+    }
     return KV_OK;
 }
 
@@ -252,6 +259,52 @@ int kv_alloc_stats(kv_alloc_t* a, int* free_blocks, int* used_blocks, int* num_s
         if (block >= a->num_blocks) return KV_ERR_INVALID_ARG;
         if (refcount) *refcount = a->refcount[block];
     }
+    return KV_OK;
+}
+
+int kv_alloc_shape(kv_alloc_t* a, int* num_blocks, int* num_kv_heads, int* head_dim,
+                   int* kv_dtype)
+{
+    if (!a) return KV_ERR_INVALID_ARG;
+    if (num_blocks) *num_blocks = a->num_blocks;
+    if (num_kv_heads) *num_kv_heads = a->num_kv_heads;
+    if (head_dim) *head_dim = a->head_dim;
+    if (kv_dtype) *kv_dtype = a->kv_dtype;
+    return KV_OK;
+}
+
+int kv_alloc_trace(kv_alloc_t* a, const int64_t* seq_ids, int n, int64_t* rows, int* count)
+{
+    if (!a || n < 0) return KV_ERR_INVALID_ARG;
+    std::vector<int64_t> ids;
+    if (seq_ids) {
+        ids.assign(seq_ids, seq_ids + n);
+        for (int64_t id : ids)
+            if (!a->seqs.count(id)) return KV_ERR_NOT_FOUND;
+    } else {
+        ids.reserve(a->seqs.size());
+        for (const auto& kv : a->seqs) ids.push_back(kv.first);
+        std::sort(ids.begin(), ids.end());
+        if ((int64_t)ids.size() > n) return KV_ERR_INVALID_ARG;
+    }
+    if (!ids.empty() && !rows) return KV_ERR_INVALID_ARG;
+    const int64_t elt = a->kv_dtype == KV_DTYPE_FP8_E4M3 ? 1 : 2;
+    const int64_t block_bytes = 2 * KV_BLOCK_SIZE * (int64_t)a->num_kv_heads * a->head_dim * elt;
+    for (size_t r = 0; r < ids.size(); ++r) {
+        const Seq& s = a->seqs.find(ids[r])->second;
+        int64_t shared = 0;
+        for (int32_t b : s.blocks) shared += a->refcount[b] > 1;
+        int64_t* row = rows + r * KV_TRACE_FIELDS;
+        row[KV_TRACE_SEQ_ID] = ids[r];
+        row[KV_TRACE_SLOT] = s.slot;
+        row[KV_TRACE_LEN] = s.len;
+        row[KV_TRACE_POSITION] = s.len;
+        row[KV_TRACE_BLOCKS] = (int64_t)s.blocks.size();
+        row[KV_TRACE_SHARED_BLOCKS] = shared;
+        row[KV_TRACE_CACHE_BYTES] = (int64_t)s.blocks.size() * block_bytes;
+        row[KV_TRACE_REORDER_SRC] = s.reorder_src;
+    }
+    if (count) *count = (int)ids.size();
     return KV_OK;
 }
 

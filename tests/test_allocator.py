@@ -210,3 +210,52 @@ def test_reorder_with_duplicates_shares_and_releases(pk):
         a.reorder([0, 1], [0, 2])                # index out of range
     with pytest.raises(pk.KVError):
         a.reorder([0, 0], [0, 1])                # repeated sequence id
+
+
+def test_trace_records_the_state_contract_fields(pk):
+    # the fields a trace keeps: request id, batch slot, length, position offset,
+    # cache shape and bytes, and the reorder permutation; checked against
+    # what the operations above imply, and a 2-layer pool's byte count
+    a = pk.BlockAllocator(64, 8, 128)
+    assert a.shape() == ((64, 8, 16, 128), pk.BF16)
+    a.add(10, 20)                          # 2 blocks
+    a.add(11, 35)                          # 3 blocks
+    a.add(12, 50)                          # 4 blocks
+    t = {r["seq_id"]: r for r in a.trace()}
+    assert [r["seq_id"] for r in a.trace()] == [10, 11, 12]
+    assert t[11] == {"seq_id": 11, "slot": -1, "len": 35, "position": 35, "blocks": 3,
+                     "shared_blocks": 0, "cache_bytes": 3 * 2 * 16 * 8 * 128 * 2,
+                     "reorder_src": -1, "mask_shape": [1, 35]}
+    # one block of K and V for one layer is the pages' per-token formula x 16
+    assert t[10]["cache_bytes"] == 2 * pk.kv_bytes(1, 1, 8, 16, 128, 2)
+    a.step([12, 10, 11], 8)
+    t = {r["seq_id"]: r for r in a.trace()}
+    assert [t[s]["slot"] for s in (12, 10, 11)] == [0, 1, 2]
+    assert [t[s]["len"] for s in (12, 10, 11)] == [51, 21, 36]
+    assert all(t[s]["position"] == t[s]["len"] for s in t)
+    # rows [A0, A1, B0] -> [B0, A1, A0] with permutation [2, 1, 0]
+    a.reorder([10, 11, 12], [2, 1, 0])
+    tr = a.trace([10, 11, 12])
+    assert [r["reorder_src"] for r in tr] == [2, 1, 0]
+    assert [r["slot"] for r in tr] == [0, 1, 2]
+    assert [r["len"] for r in tr] == [51, 36, 21]
+    # beam duplication: both rows share every block
+    a.reorder([10, 11], [0, 0])
+    tr = a.trace([10, 11])
+    assert tr[0]["shared_blocks"] == tr[0]["blocks"] == tr[1]["shared_blocks"] == 4
+    a.fork(12, 13, 16)
+    assert a.trace([13])[0] == {"seq_id": 13, "slot": -1, "len": 16, "position": 16,
+                                "blocks": 1, "shared_blocks": 1,
+                                "cache_bytes": 2 * 16 * 8 * 128 * 2, "reorder_src": -1,
+                                "mask_shape": [1, 16]}
+    lines = a.dump().splitlines()
+    import json
+    head = json.loads(lines[0])
+    assert head["kv_shape"] == [64, 8, 16, 128] and head["num_seqs"] == 4
+    assert [json.loads(x)["seq_id"] for x in lines[1:]] == [10, 11, 12, 13]
+    with pytest.raises(pk.KVError):
+        a.trace([99])
+    f8 = pk.BlockAllocator(4, 2, 64, kv_dtype=pk.FP8_E4M3)
+    f8.add(0, 17)
+    assert f8.trace()[0]["cache_bytes"] == 2 * 2 * 16 * 2 * 64 * 1
+    assert f8.trace([]) == [] and pk.BlockAllocator(2, 1, 64).trace() == []

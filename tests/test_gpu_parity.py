@@ -333,6 +333,37 @@ def test_bad_inputs_are_flagged_not_faulted():
     assert float(x.sum()) == 8.0
 
 
+def test_context_longer_than_its_table_row_is_flagged_and_clamped():
+    """A context length past its block-table row (the context-limit overflow
+    case) or below zero is reported as KV_DEVERR_CONTEXT_TOO_LONG with the bad
+    length, clamped into [0, 16 * max_blocks_per_seq], and nothing faults."""
+    import paged_kv_cache_21_gb300 as pk
+    # sequence 2 fills its 7-entry row, so the clamped length reads valid blocks
+    case = workloads.make_custom(3, 8, 2, 128, [40, 64, 100], seed=21)
+    mb = case.block_tables.shape[1]
+    assert mb == 7 and (case.block_tables[2] >= 0).all()
+    _, kc, vc = H.gpu_step(case)
+    pk.get_device_error()
+    okc, ovc = H.oracle_caches(case)
+    bt = torch.from_numpy(case.block_tables).cuda()
+    q64 = oracle.bf16_bits_to_f64(bf16_bits(case.q))
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    for bad, clamped in ((16 * mb + 5, 16 * mb), (-3, 0)):
+        lens = case.context_lens.copy()
+        lens[2] = bad
+        out = torch.empty((case.B, case.Hq, case.D), dtype=torch.float32, device="cuda")
+        pk.paged_decode_attention(out, case.q.cuda(), kc, vc, bt, torch.from_numpy(lens).cuda(),
+                                  case.scale, ws)
+        torch.cuda.synchronize()
+        flags, detail = pk.get_device_error()
+        assert flags == pk.DEVERR_CONTEXT_TOO_LONG and detail == bad
+        ref_lens = lens.copy()
+        ref_lens[2] = clamped
+        ref = oracle.paged_attention(q64, okc, ovc, case.block_tables, ref_lens, case.scale)
+        assert np.max(np.abs(out.cpu().numpy() - ref)) < 2e-3
+    assert pk.get_device_error()[0] == 0
+
+
 def test_workspace_needs_no_initialisation():
     """Garbage-filled workspace, then the same workspace reused: the in-kernel
     merge counters must start from zero arrivals each launch."""

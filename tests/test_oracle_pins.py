@@ -435,3 +435,36 @@ def test_fp8_attention_reads_dequantised_values():
     # and quantisation error against the unquantised values is small
     ref = oracle.attention_direct(q, bf16_exact(Kf), bf16_exact(Vf), 0.125)
     assert np.max(np.abs(out - ref)) < 0.1
+
+
+# ------------------------------------------------- cached vs naive decoding
+
+def test_token_by_token_generation_cached_equals_naive(golden):
+    """A 100-token generation run both ways: the naive decoder recomputes
+    causal attention over the whole prefix at every step, the cached one
+    appends the new K/V into a paged pool (slots from the block table) and
+    attends only the new query.  The pages fix the work of each (query rows
+    attended) and require the two paths to give the same outputs."""
+    (N, naive_want, cached_want), = golden("attention_op_count.txt")
+    rng = np.random.default_rng(77)
+    D, scale = 16, 0.25
+    Q = bf16_exact(rng.standard_normal((N, D)))
+    K = bf16_exact(rng.standard_normal((N, D)))
+    V = bf16_exact(rng.standard_normal((N, D)))
+    nb = -(-N // BS)
+    NB = nb + 5
+    bt = rng.permutation(NB)[:nb].astype(np.int32).reshape(1, nb)
+    kc = bits_of(rng.standard_normal((NB, 1, BS, D)))     # stale contents everywhere
+    vc = bits_of(rng.standard_normal((NB, 1, BS, D)))
+    naive_ops = cached_ops = 0
+    for t in range(N):
+        rows = oracle.causal_attention(Q[:t + 1], K[:t + 1], V[:t + 1], scale)
+        naive_ops += rows.shape[0]
+        slot = oracle.slot_mapping(bt, [0], [t])
+        assert oracle.append(kc, vc, bits_of(K[t]).reshape(1, 1, D),
+                             bits_of(V[t]).reshape(1, 1, D), slot, oracle.BF16) == 0
+        out = run_oracle_single(Q[t], kc, vc, bt[0], t + 1, scale)
+        cached_ops += 1
+        np.testing.assert_allclose(out[0, 0], rows[t], rtol=0, atol=1e-12)
+    assert (naive_ops, cached_ops) == (naive_want, cached_want)
+    assert naive_ops == N * (N + 1) // 2
