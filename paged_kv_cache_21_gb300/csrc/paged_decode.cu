@@ -56,6 +56,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -76,8 +77,12 @@ constexpr int kWarpStageBytesBf16 = 24576;
 constexpr int kWarpStageBytesFp8 = 24576;
 constexpr int kMinCtasBf16 = 1;
 constexpr int kMinCtasFp8 = 1;
-constexpr int kMinBlocksPerWarp = 16;            // do not split below 256 tokens per warp
-constexpr int kMinBlocksPerWarpChunk = 4;        // the same for the prefix chunk phase
+// Minimum range of a warp.  Sequence phase: at most 16 blocks (256 tokens);
+// with a narrow block table, ceil(max_blocks / 8) but at least 2, so that a
+// small problem spreads over more warps while every pair still meets about
+// kMergeDirect ranges (the merge's one-round-trip path).
+constexpr int kMinBlocksPerWarp = 16;
+constexpr int kMinBlocksPerWarpChunk = 4;        // the prefix chunk phase
 constexpr long long kWaitLimit = 1LL << 31;      // ~1 s of SM clocks
 
 template <int D, bool FP8>
@@ -132,6 +137,7 @@ struct DecodeParams {
     uint8_t* v_cache;
     int B, Hq, Hkv, G, max_blocks, num_blocks;
     int warps_total;
+    int min_q1;              // minimum range of a warp in the sequence phase
     float sl2;               // scale * log2(e) (* k_scale)
     float v_scale;
     float k_qscale, v_qscale;    // quantisation scales of the fused append (E4M3)
@@ -838,7 +844,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
         const int nc = NR == 2 ? p.nc : 0;
         const int s_lo = ph == 0 ? 0 : nc;
         const int ns = ph == 0 ? nc : nc + p.B;           // streams [s_lo, ns)
-        const int min_q = ph == 0 ? kMinBlocksPerWarpChunk : kMinBlocksPerWarp;
+        const int min_q = ph == 0 ? kMinBlocksPerWarpChunk : p.min_q1;
         const int slot_base = ph == 0 ? 0 : p.slot_base;
 
         // ---- 1. total work and this warp's range --------------------------------
@@ -1552,6 +1558,8 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.max_blocks = max_blocks_per_seq;
     dp.num_blocks = num_blocks;
     dp.warps_total = warps_total;
+    dp.min_q1 = std::min(kMinBlocksPerWarp,
+                         std::max(2, (max_blocks_per_seq + kMergeDirect - 1) / kMergeDirect));
     dp.sl2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
     dp.v_scale = fp8 ? v_scale : 1.f;
     dp.k_qscale = k_scale;

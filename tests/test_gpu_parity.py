@@ -247,6 +247,58 @@ def test_block_permutation_bitwise_invariant_and_deterministic():
     assert torch.equal(out2.view(torch.int16), out3.view(torch.int16))
 
 
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_pool_past_4_gib_with_block_ids_at_its_top(kv_dtype):
+    """Largest addresses: the same logical cache placed in a pool of more than
+    4 GiB per cache tensor, on block ids at its top end (the last id
+    included).  The fused step (append + attention, early inputs) must give
+    the same bits as on a compact pool, write the same cache bytes, and agree
+    with the oracle; a block copy between two high ids moves the right bytes."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(5, 32, 8, 128, [300, 1000, 17, 2500, 1], kv_dtype=kv_dtype,
+                                 seed=61)
+    out_ref, kc, vc = H.gpu_step(case, fused=True, early_inputs=True)
+    okc, ovc = H.oracle_caches(case)
+    assert np.array_equal(cache_bits(kc), okc) and np.array_equal(cache_bits(vc), ovc)
+    H.compare(case, out_ref, H.oracle_step(case, okc, ovc), what="compact pool")
+
+    block_bytes = case.Hkv * 16 * case.D * (2 if kv_dtype == workloads.BF16 else 1)
+    NB_big = (9 << 29) // block_bytes + 1000            # 4.5 GiB + 1000 blocks per cache
+    rng = np.random.default_rng(62)
+    off = np.concatenate([[0], 1 + rng.permutation(4 * case.num_blocks)[:case.num_blocks - 1]])
+    remap = (NB_big - 1 - off).astype(np.int64)          # distinct, block 0 -> the last id
+    assert remap.min() * block_bytes >= 1 << 32
+    cdt = torch.bfloat16 if kv_dtype == workloads.BF16 else torch.uint8
+    kb = torch.zeros((NB_big, case.Hkv, 16, case.D), dtype=cdt, device="cuda")
+    vb = torch.zeros_like(kb)
+    c = np.arange(case.num_blocks * 16, dtype=np.int64)
+    slots = torch.from_numpy(remap[c // 16] * 16 + c % 16).cuda()
+    pk.kv_append(case.pool_k.cuda(), case.pool_v.cuda(), kb, vb, slots, case.k_scale,
+                 case.v_scale)
+    bt_big = np.where(case.block_tables >= 0, remap[np.maximum(case.block_tables, 0)], -1)
+    out_big = torch.empty_like(out_ref)
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D, kv_dtype)
+    pk.paged_decode(out_big, case.q.cuda(), kb, vb, torch.from_numpy(bt_big.astype(np.int32)).cuda(),
+                    torch.from_numpy(case.context_lens).cuda(), case.scale, ws, case.k_scale,
+                    case.v_scale, k_new=case.k_new.cuda(), v_new=case.v_new.cuda(),
+                    early_inputs=True)
+    torch.cuda.synchronize()
+    assert pk.get_device_error()[0] == 0
+    assert torch.equal(out_big.view(torch.int16), out_ref.view(torch.int16))
+    rt = torch.from_numpy(remap).cuda()
+    assert torch.equal(kb[rt].view(torch.uint8), kc.view(torch.uint8))
+    assert torch.equal(vb[rt].view(torch.uint8), vc.view(torch.uint8))
+    # copy-on-write between two high ids: the top block onto a free one
+    free_id = int(np.setdiff1d(np.arange(NB_big - 10, NB_big), remap)[0])
+    pk.kv_copy_blocks(kb, vb, torch.tensor([NB_big - 1], dtype=torch.int32, device="cuda"),
+                      torch.tensor([free_id], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(kb[free_id].view(torch.uint8), kc[0].view(torch.uint8))
+    assert torch.equal(vb[free_id].view(torch.uint8), vc[0].view(torch.uint8))
+    del kb, vb
+    torch.cuda.empty_cache()
+
+
 def test_allocator_driven_steps_with_copy_on_write():
     """Sequences created, forked (shared prefix, copy-on-write) and stepped by
     the host allocator; GPU copies/appends/attends; oracle replays the same
