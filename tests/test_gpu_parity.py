@@ -705,3 +705,18 @@ def test_pinned_host_buffers_read_in_place():
     assert torch.equal(hs.out.view(torch.int16), out_d.cpu().view(torch.int16))
     assert torch.equal(kc.view(torch.int16), kc_d.view(torch.int16))
     assert torch.equal(vc.view(torch.int16), vc_d.view(torch.int16))
+
+
+def test_readme_usage_example_runs():
+    """The README's usage block, executed as written."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "README.md")).read()
+    blocks = re.findall(r"```python\n(.*?)```", text, flags=re.S)
+    assert blocks, "no python block in README.md"
+    env = {}
+    exec(compile(blocks[0], "README.md", "exec"), env)
+    torch.cuda.synchronize()
+    assert torch.isfinite(env["out"].float()).all()
+    assert list(env["lens"]) == [1, 1]
