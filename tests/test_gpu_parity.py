@@ -718,5 +718,6 @@ def test_readme_usage_example_runs():
     env = {}
     exec(compile(blocks[0], "README.md", "exec"), env)
     torch.cuda.synchronize()
-    assert torch.isfinite(env["out"].float()).all()
     assert list(env["lens"]) == [1, 1]
+    # one key per sequence: each query head returns its KV head's new V exactly
+    assert torch.equal(env["out"], env["v_new"].repeat_interleave(4, dim=1))
