@@ -373,6 +373,67 @@ def test_allocator_driven_steps_with_copy_on_write():
     assert alloc.stats()[0] == NB
 
 
+def test_cancelled_request_frees_blocks_for_a_new_one():
+    """Request cancellation mid-batch (mask/KV page, implementation and
+    verification procedure): a sequence is freed between steps, a new request
+    takes its blocks (stale K/V still in them) and the batch goes on through
+    the fused step with early inputs.  Every step matches the oracle on the
+    same tables; stale slots past a length must get no weight."""
+    import paged_kv_cache_21_gb300 as pk
+    Hq, Hkv, D, NB, MB = 8, 2, 128, 24, 8
+    alloc = pk.BlockAllocator(NB, Hkv, D)
+    g = torch.Generator().manual_seed(41)
+    kc = torch.zeros((NB, Hkv, 16, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    okc = np.zeros((NB, Hkv, 16, D), dtype=np.uint16)
+    ovc = np.zeros_like(okc)
+    scale = 1 / math.sqrt(D)
+
+    def prefill(sid, n):
+        alloc.add(sid, n)
+        _, row = alloc.info(sid)
+        k = torch.randn((n, Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((n, Hkv, D), generator=g).to(torch.bfloat16)
+        sl = np.array([row[p // 16] * 16 + p % 16 for p in range(n)], dtype=np.int64)
+        pk.kv_append(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(sl).cuda())
+        oracle.append(okc, ovc, bf16_bits(k), bf16_bits(v), sl, oracle.BF16)
+        return set(int(b) for b in row)
+
+    def decode(ids, steps):
+        ws = pk.alloc_workspace(len(ids), Hq, Hkv, D)
+        for _ in range(steps):
+            slots, bt, lens, (cs, _) = alloc.step(ids, MB)
+            assert len(cs) == 0
+            k = torch.randn((len(ids), Hkv, D), generator=g).to(torch.bfloat16)
+            v = torch.randn((len(ids), Hkv, D), generator=g).to(torch.bfloat16)
+            q = torch.randn((len(ids), Hq, D), generator=g).to(torch.bfloat16)
+            out = torch.empty((len(ids), Hq, D), dtype=torch.float32, device="cuda")
+            pk.paged_decode(out, q.cuda(), kc, vc, torch.from_numpy(bt).cuda(),
+                            torch.from_numpy(lens).cuda(), scale, ws, k_new=k.cuda(),
+                            v_new=v.cuda(), early_inputs=True)
+            oracle.append(okc, ovc, bf16_bits(k), bf16_bits(v), slots, oracle.BF16)
+            ref = oracle.paged_attention(oracle.bf16_bits_to_f64(bf16_bits(q)), okc, ovc, bt,
+                                         lens, scale)
+            torch.cuda.synchronize()
+            assert np.array_equal(cache_bits(kc), okc)
+            assert np.max(np.abs(out.cpu().numpy() - ref)) < 2e-3
+
+    prefill(0, 30)
+    cancelled = prefill(1, 45)
+    prefill(2, 20)
+    decode([0, 1, 2], 3)
+    alloc.free(1)                                  # cancelled after 48 tokens: 3 blocks
+    assert alloc.stats()[2] == 2
+    fresh = prefill(3, 40)                         # takes freed blocks, stale data inside
+    assert fresh & cancelled
+    decode([0, 2, 3], 4)
+    decode([3, 0], 2)                              # the batch shrinks and reorders
+    assert pk.get_device_error()[0] == 0
+    for sid in (0, 2, 3):
+        alloc.free(sid)
+    assert alloc.stats()[0] == NB
+
+
 def test_bad_inputs_are_flagged_not_faulted():
     """Out-of-range slots and block ids are skipped and reported through the
     device error word; the context stays usable."""
