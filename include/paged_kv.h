@@ -288,7 +288,10 @@ int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads
  * while the previous kernel on the stream drains, and waits on the device for
  * it to finish before reading or writing any buffer.  Deterministic: the same
  * inputs on the same device give bit-identical outputs, whatever the physical
- * block ids.  `out` must be 16-byte aligned. */
+ * block ids.  The split of the work over warps, and so the rounding order,
+ * follows the device's SM count and max_blocks_per_seq (a narrow table lets
+ * short sequences spread over more warps); results agree within the
+ * tolerance across either.  `out` must be 16-byte aligned. */
 int paged_decode_attention(void* out, int out_dtype, const void* q, const void* k_cache,
                            const void* v_cache, int kv_dtype, float k_scale, float v_scale,
                            int num_blocks, const int32_t* block_tables, int max_blocks_per_seq,
