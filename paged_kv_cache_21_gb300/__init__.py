@@ -486,6 +486,13 @@ class DecodeStepStaging:
     alternate, so step i+1's upload and step i's download overlap the kernels
     of the steps around them.
 
+    The compute stream waits for each upload through an event, which also
+    ends the programmatic overlap of consecutive steps.  With
+    ``host_ordered=True`` the host instead blocks until the step's upload has
+    finished before launching its kernels (the upload was queued a step
+    earlier, so the host stays about one step ahead): the compute stream then
+    holds only kernel launches and consecutive steps keep their overlap.
+
     With ``zero_copy=True`` there are no copies and no device slots: the
     kernels read the step's inputs from the pinned host slot and write the
     output into it directly (over NVLink-C2C on a Grace-Blackwell node), and
@@ -502,10 +509,12 @@ class DecodeStepStaging:
         pass
 
     def __init__(self, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks,
-                 kv_dtype=BF16, device=None, out_dtype=None, slots=2, zero_copy=False):
+                 kv_dtype=BF16, device=None, out_dtype=None, slots=2, zero_copy=False,
+                 host_ordered=False):
         import torch
         self.device = torch.device(device or "cuda")
         self.zero_copy = bool(zero_copy)
+        self.host_ordered = bool(host_ordered)
         B, Hq, Hkv, D = num_seqs, num_q_heads, num_kv_heads, head_dim
         parts = [("q", (B, Hq, D), torch.bfloat16), ("k_new", (B, Hkv, D), torch.bfloat16),
                  ("v_new", (B, Hkv, D), torch.bfloat16),
@@ -577,12 +586,16 @@ class DecodeStepStaging:
             ev["computed"].record(s)
             return
         up, down = self.upload_stream, self.download_stream
-        # the device slot is free once its previous step has been computed
-        up.wait_event(ev["computed"])
+        # the device slot is free once its previous step has been computed and
+        # its output downloaded (the download follows the computation)
+        up.wait_event(ev["downloaded"])
         with torch.cuda.stream(up):
             d.raw.copy_(h.raw, non_blocking=True)
             ev["uploaded"].record(up)
-        s.wait_event(ev["uploaded"])
+        if self.host_ordered:
+            ev["uploaded"].synchronize()
+        else:
+            s.wait_event(ev["uploaded"])
         # the inputs arrive by a copy joined through an event, and the kernel
         # before is the previous step's: the early reads are safe
         paged_decode(d.out, d.q, k_cache, v_cache, d.block_tables, d.context_lens, scale,

@@ -601,15 +601,18 @@ def test_beam_reorder_and_duplication_through_the_kernels():
     assert alloc.stats()[0] == NB
 
 
-def test_staged_host_steps_match_device_step():
+@pytest.mark.parametrize("host_ordered", [False, True])
+def test_staged_host_steps_match_device_step(host_ordered):
     """DecodeStepStaging (per step: one H2D copy of every input on a copy
     stream, fused step, one D2H copy; two alternating slots) gives the same
-    bits as the fused step on device inputs, step after step."""
+    bits as the fused step on device inputs, step after step, whether the
+    compute stream or the host waits for each upload."""
     import paged_kv_cache_21_gb300 as pk
     case = workloads.make_custom(5, 32, 8, 128, [1, 300, 4097, 9000, 20], seed=81)
     out_ref, kc, vc = H.gpu_step(case, fused=True)
     # the fused step already appended the new tokens; rerunning rewrites them identically
-    stg = pk.DecodeStepStaging(case.B, case.Hq, case.Hkv, case.D, case.max_blocks)
+    stg = pk.DecodeStepStaging(case.B, case.Hq, case.Hkv, case.D, case.max_blocks,
+                               host_ordered=host_ordered)
     for i in range(5):
         stg.ready_for_input(i)
         hs = stg.host(i)
