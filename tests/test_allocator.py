@@ -137,46 +137,69 @@ def test_random_operations_keep_pool_invariants(pk):
     NB = 200
     a = pk.BlockAllocator(NB, 2, 64)
     lens = {}
+    slot = {}                    # model of the trace: batch row, last reorder source
+    rsrc = {}
     next_id = 0
     for _ in range(1500):
-        op = rng.integers(0, 4)
+        op = rng.integers(0, 5)
         try:
             if op == 0:
                 ln = int(rng.integers(0, 80))
                 a.add(next_id, ln)
-                lens[next_id] = ln
+                lens[next_id], slot[next_id], rsrc[next_id] = ln, -1, -1
                 next_id += 1
             elif op == 1 and lens:
                 sid = int(rng.choice(list(lens)))
                 a.free(sid)
-                del lens[sid]
+                del lens[sid], slot[sid], rsrc[sid]
             elif op == 2 and lens:
                 sid = int(rng.choice(list(lens)))
                 sl = int(rng.integers(0, lens[sid] + 1))
                 a.fork(sid, next_id, sl)
-                lens[next_id] = sl
+                lens[next_id], slot[next_id], rsrc[next_id] = sl, -1, -1
                 next_id += 1
             elif op == 3 and lens:
                 ids = rng.choice(list(lens), size=min(len(lens), 5), replace=False)
                 slots, bt, ln, _ = a.step(ids, 64)
                 for i, sid in enumerate(ids):
                     lens[int(sid)] += 1
+                    slot[int(sid)] = i
                     assert ln[i] == lens[int(sid)]
                 np.testing.assert_array_equal(
                     slots, oracle.slot_mapping(bt, np.arange(len(ids)), ln.astype(np.int64) - 1))
+            elif op == 4 and lens:
+                ids = [int(x) for x in rng.choice(list(lens), size=min(len(lens), 4),
+                                                  replace=False)]
+                src = rng.integers(0, len(ids), size=len(ids))
+                a.reorder(ids, src)
+                old = [lens[x] for x in ids]
+                for i, sid in enumerate(ids):
+                    lens[sid], slot[sid], rsrc[sid] = old[src[i]], i, int(src[i])
         except pk.KVError as e:
             assert e.code in (pk.KV_ERR_OUT_OF_BLOCKS, pk.KV_ERR_INVALID_ARG)
         free, used, nseq, _ = a.stats()
         assert free + used == NB and nseq == len(lens)
     holders = {}
+    rows = {}
     for sid, ln in lens.items():
         got_len, row = a.info(sid)
         assert got_len == ln and len(row) == -(-ln // 16)
+        rows[sid] = row
         for b in row:
             holders[int(b)] = holders.get(int(b), 0) + 1
     for b in range(NB):
         assert a.stats(b)[3] == holders.get(b, 0)
     assert a.stats()[1] == len(holders)
+    # the debug trace agrees with the model, field by field
+    trace = a.trace()
+    assert [r["seq_id"] for r in trace] == sorted(lens)
+    for r in trace:
+        sid = r["seq_id"]
+        nb = len(rows[sid])
+        assert (r["slot"], r["reorder_src"]) == (slot[sid], rsrc[sid])
+        assert r["len"] == r["position"] == lens[sid] and r["mask_shape"] == [1, lens[sid]]
+        assert r["blocks"] == nb and r["cache_bytes"] == nb * 2 * 16 * 2 * 64 * 2
+        assert r["shared_blocks"] == sum(holders[int(b)] > 1 for b in rows[sid])
 
 
 def test_reorder_follows_the_row_permutation(pk):
