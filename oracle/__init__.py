@@ -22,6 +22,12 @@ Contents
   mask and KV cache inference", sections "State of scaled dot-product
   attention" and "Causal mask and future positions").  Its last row is what
   one decode step over the same tokens must return.
+* ``split_partials`` / ``lse_merge`` -- split-KV: the keys cut into ranges,
+  each range's normalised output with its log-sum-exp, then the combine
+  out = sum_i e^(lse_i - M) o_i / sum_i e^(lse_i - M), M = max_i lse_i.  Both
+  are derived from the running (max, sum) rule of the lesson's "Numerical
+  trick" (the pages give no split-KV listing); they must equal
+  ``attention_direct`` for any cut.
 * ``paged_attention`` / ``append`` / E4M3 and bfloat16 conversions -- thin
   ctypes wrappers over ``oracle.c`` (float64 C, OpenMP over sequence x KV head).
 """
@@ -230,6 +236,40 @@ def tiled_softmax_attention(q, K, V, scale, tile=4):
         o = o * carry + (e[:, None] * V[start:start + tile]).sum(axis=0)
         m = m_new
     return o / s
+
+
+def split_partials(q, K, V, scale, bounds):
+    """Cut the keys at ``bounds`` (increasing indices from 0 to L) and return,
+    per range [a, b), the normalised output o = sum_j w_j V_j / sum_j w_j and
+    lse = m + log(sum_j e^(z_j - m)) with z = scale * K q, m = max z.  An
+    empty range gives (zeros, -inf)."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    parts = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b <= a:
+            parts.append((np.zeros(V.shape[1]), -np.inf))
+            continue
+        z = scale * (K[a:b] @ q)
+        m = float(z.max())
+        w = np.exp(z - m)
+        s = float(w.sum())
+        parts.append(((w[:, None] * V[a:b]).sum(axis=0) / s, m + float(np.log(s))))
+    return parts
+
+
+def lse_merge(parts):
+    """Combine (o_i, lse_i) partials: weights e^(lse_i - M), M = max lse_i;
+    partials with lse = -inf (no keys) get weight 0.  No partial with keys
+    gives zeros."""
+    lse = np.array([p[1] for p in parts], dtype=np.float64)
+    if not np.isfinite(lse).any():
+        return np.zeros_like(np.asarray(parts[0][0], dtype=np.float64))
+    M = lse[np.isfinite(lse)].max()
+    w = np.where(np.isfinite(lse), np.exp(lse - M), 0.0)
+    o = np.stack([np.asarray(p[0], dtype=np.float64) for p in parts])
+    return (w[:, None] * o).sum(axis=0) / w.sum()
 
 
 def causal_mask(L):

@@ -468,3 +468,48 @@ def test_token_by_token_generation_cached_equals_naive(golden):
         np.testing.assert_allclose(out[0, 0], rows[t], rtol=0, atol=1e-12)
     assert (naive_ops, cached_ops) == (naive_want, cached_want)
     assert naive_ops == N * (N + 1) // 2
+
+
+# ---------------------------------------------------- split-KV and the merge
+
+@pytest.mark.parametrize("L", [1, 17, 100, 513])
+def test_split_partials_merge_to_direct_attention(L):
+    """Any cut of the keys, empty ranges included, merged by log-sum-exp,
+    equals one-shot attention; one range is the library's logsumexp."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(300 + L)
+    D = 32
+    q = rng.standard_normal(D)
+    K = rng.standard_normal((L, D))
+    V = rng.standard_normal((L, D))
+    scale = 0.3
+    direct = oracle.attention_direct(q, K, V, scale)
+    (o1, lse1), = oracle.split_partials(q, K, V, scale, [0, L])
+    np.testing.assert_allclose(o1, direct, rtol=0, atol=1e-13)
+    assert abs(lse1 - logsumexp(scale * (K @ q))) < 1e-12
+    for trial in range(5):
+        cuts = np.sort(rng.integers(0, L + 1, size=rng.integers(1, 9)))
+        bounds = [0] + [int(c) for c in cuts] + [L]      # repeats give empty ranges
+        parts = oracle.split_partials(q, K, V, scale, bounds)
+        merged = oracle.lse_merge(parts)
+        np.testing.assert_allclose(merged, direct, rtol=0, atol=1e-12)
+        perm = rng.permutation(len(parts))
+        np.testing.assert_allclose(oracle.lse_merge([parts[i] for i in perm]), merged,
+                                   rtol=0, atol=1e-14)
+
+
+def test_merge_is_stable_for_large_scores_and_empty_inputs():
+    """Scores near 1e3 overflow e^z; the merge must still equal the direct
+    result.  With no keys at all the merge gives zeros (the empty-context
+    reading)."""
+    rng = np.random.default_rng(310)
+    D, L = 16, 64
+    q = rng.standard_normal(D) * 40
+    K = rng.standard_normal((L, D)) * 40
+    V = rng.standard_normal((L, D))
+    direct = oracle.attention_direct(q, K, V, 1.0)
+    assert np.all(np.isfinite(direct))
+    merged = oracle.lse_merge(oracle.split_partials(q, K, V, 1.0, [0, 10, 30, 31, 64]))
+    np.testing.assert_allclose(merged, direct, rtol=0, atol=1e-12)
+    empty = oracle.split_partials(q, K[:0], V[:0], 1.0, [0, 0, 0])
+    np.testing.assert_array_equal(oracle.lse_merge(empty), np.zeros(D))
