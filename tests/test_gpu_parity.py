@@ -180,6 +180,17 @@ def test_narrow_tables_spread_over_more_warps(max_len, kv_dtype):
                early_inputs=True)
 
 
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+@pytest.mark.parametrize("lens", [[20000, 20000], [100000]])
+def test_one_pair_split_over_hundreds_of_warps(lens, kv_dtype):
+    """A few long sequences with one KV head: ranges of 16 blocks cut a pair
+    into ~80 or ~390 partials, so the merge stages them in several rounds of
+    64 (the path beyond one round trip)."""
+    case = workloads.make_custom(len(lens), 8, 1, 128, lens, kv_dtype=kv_dtype, seed=len(lens))
+    check_case(case, what="%d partials" % (lens[0] // 256))
+    check_case(case, what="fused early", fused=True, early_inputs=True)
+
+
 def test_group_sizes_two_three_five_seven():
     for G in (2, 3, 5, 7):
         case = workloads.make_custom(3, 3 * G, 3, 128, [40, 700, 2000], seed=G)
@@ -495,8 +506,9 @@ def test_context_longer_than_its_table_row_is_flagged_and_clamped():
 
 
 def test_workspace_needs_no_initialisation():
-    """Garbage-filled workspace, then the same workspace reused: the in-kernel
-    merge counters must start from zero arrivals each launch."""
+    """Garbage-filled workspace, then the same workspace reused: every launch
+    writes the pair table and the partial slots it reads, so nothing depends
+    on what the workspace held before."""
     import paged_kv_cache_21_gb300 as pk
     case = workloads.make_custom(5, 32, 8, 128, [3000, 9000, 17, 20000, 513], seed=44)
     ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
