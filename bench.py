@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "b55e054ed277220303544dfc712b440437f10bc4ba6a77872a817685a82c1faa",
-           "bytes_per_launch": 1087720448,
+TRAFFIC = {"kernel_sha256": "6ecf58d3f34b87462dcaf8b07cb4c7b6227e1c4cfc7641feff2d52d85708e653",
+           "bytes_per_launch": 1088880640,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,147,904 B + 2,782,208 B), scaled x4 by units processed "
+                     "(269,146,368 B + 3,073,792 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 

@@ -36,9 +36,14 @@
  *     the [heads, seq, head_dim] order inside it is the tensor shape of "KV
  *     Cache" (heepie.pages.dev), section "Tensor".
  *   - Supported shapes: head_dim 64 or 128; num_q_heads a multiple of
- *     num_kv_heads with group size G = num_q_heads / num_kv_heads in 1..8
- *     ("KV cache complete guide", section "(2) GQA": MHA G=1, GQA, MQA).
- *     Query head h reads KV head h / G.
+ *     num_kv_heads with group size G = num_q_heads / num_kv_heads
+ *     ("KV cache complete guide", section "(2) GQA": MHA G=1, GQA, and MQA,
+ *     one KV head for all query heads).  G may be 1..16, or up to 128 when
+ *     G / 2^k <= 16 for some k <= 3 divides evenly (e.g. 24, 32, 64, 128;
+ *     not 17 or 34: KV_ERR_UNSUPPORTED).  Query head h reads KV head h / G.
+ *     Groups above 8 rows run the two-row-tile kernel; groups above 16 are
+ *     cut into 2^k sub-groups that each read the KV head's tiles (the
+ *     repeats are served mostly from L2).  Prefix chunks need G <= 8.
  */
 #ifndef PAGED_KV_H
 #define PAGED_KV_H
@@ -406,7 +411,8 @@ int paged_decode_attention_noalloc(void* out, int out_dtype, const void* q, cons
  *     a chunk's P is its shortest member run; chunks with fewer than two
  *     members or P < min_blocks are dropped (their sequences get -1).
  * chunks must hold num_seqs / 2 rows (the most chunks possible); seq_chunk
- * num_seqs entries.  group_size = num_q_heads / num_kv_heads (1..8).
+ * num_seqs entries.  group_size = num_q_heads / num_kv_heads (1..8: a chunk
+ * packs at least two members' rows into one 16-row tile).
  * Returns KV_OK and *num_chunks, or KV_ERR_INVALID_ARG. */
 int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* context_lens, int num_seqs, int group_size, int min_blocks,

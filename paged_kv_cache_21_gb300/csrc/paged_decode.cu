@@ -138,6 +138,7 @@ struct DecodeParams {
     int B, Hq, Hkv, G, max_blocks, num_blocks;
     int warps_total;
     int min_q1;              // minimum range of a warp in the sequence phase
+    int hshift;              // a KV head serves 1 << hshift virtual heads of G rows
     float sl2;               // scale * log2(e) (* k_scale)
     float v_scale;
     float k_qscale, v_qscale;    // quantisation scales of the fused append (E4M3)
@@ -633,6 +634,8 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, bool chunk, int sc
     const int g = lane >> 2;
     if (!chunk) {
         load_q_row<D, FP8>(p, sc, h * p.G + g, g < p.G, lane, qf.a0, qf.a2);
+        if constexpr (NR == 2)
+            load_q_row<D, FP8>(p, sc, h * p.G + g + 8, g + 8 < p.G, lane, qf.a1, qf.a3);
         return;
     }
 #pragma unroll
@@ -708,26 +711,30 @@ __device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, in
         mb[r] = __shfl_sync(kFull, m[r], 8 * t + 4);
     }
     if (!sg.chunk && sg.base == 0 && sg.first == 0 && sg.last == sg.end - 1) {
-        const int ha = 2 * t, hb = 2 * t + 1;
-        const float ia = la[0] > 0.f ? p.v_scale / la[0] : 0.f;
-        const float ib = lb[0] > 0.f ? p.v_scale / lb[0] : 0.f;
         const size_t row = (size_t)sg.s * p.Hq + (size_t)sg.h * p.G;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
+        for (int r = 0; r < NR; ++r) {
+            if (r >= sg.nr) break;
+            const int ha = 8 * r + 2 * t, hb = ha + 1;
+            const float ia = la[r] > 0.f ? p.v_scale / la[r] : 0.f;
+            const float ib = lb[r] > 0.f ? p.v_scale / lb[r] : 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int d = out_dim<D, FP8>(i, g, half);
-                if (ha < p.G) {
-                    const float v = o[0][i][2 * half] * ia;
-                    const size_t idx = (row + ha) * D + d;
-                    if (p.out_f32) reinterpret_cast<float*>(p.out)[idx] = v;
-                    else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
-                }
-                if (hb < p.G) {
-                    const float v = o[0][i][2 * half + 1] * ib;
-                    const size_t idx = (row + hb) * D + d;
-                    if (p.out_f32) reinterpret_cast<float*>(p.out)[idx] = v;
-                    else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+            for (int i = 0; i < D / 16; ++i) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int d = out_dim<D, FP8>(i, g, half);
+                    if (ha < p.G) {
+                        const float v = o[r][i][2 * half] * ia;
+                        const size_t idx = (row + ha) * D + d;
+                        if (p.out_f32) reinterpret_cast<float*>(p.out)[idx] = v;
+                        else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                    }
+                    if (hb < p.G) {
+                        const float v = o[r][i][2 * half + 1] * ib;
+                        const size_t idx = (row + hb) * D + d;
+                        if (p.out_f32) reinterpret_cast<float*>(p.out)[idx] = v;
+                        else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                    }
                 }
             }
         }
@@ -777,8 +784,10 @@ __device__ __forceinline__ void append_patch(const DecodeParams& p, int s, int h
         const bool isv = lane >= CH;
         const int c = isv ? lane - CH : lane;
         const int r = (L - 1) & (kBlock - 1);
-        const size_t src = ((size_t)s * p.Hkv + h) * D + 8 * c;
-        const size_t dst = (((size_t)id * p.Hkv + h) * kBlock + r) * D + 8 * c;
+        // cache and new tokens are indexed by the physical KV head
+        const int Hp = p.Hkv >> p.hshift, hp = h >> p.hshift;
+        const size_t src = ((size_t)s * Hp + hp) * D + 8 * c;
+        const size_t dst = (((size_t)id * Hp + hp) * kBlock + r) * D + 8 * c;
         const uint4 x = __ldg(reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src));
         uint8_t* cache = isv ? p.v_cache : p.k_cache;
         const uint32_t sb = isv ? vst : kst;
@@ -964,7 +973,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                 if (valid) {
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(bar, (uint32_t)G::STAGE);
-                    const int z = id * p.Hkv + h;
+                    const int z = id * (p.Hkv >> p.hshift) + (h >> p.hshift);
                     // KV tiles are read once per step: keep them from evicting
                     // the block tables, queries and partials from L2
                     const uint64_t pol = l2_evict_first_policy();
@@ -1150,7 +1159,8 @@ struct MergeParams {
 // terms of up to 64 partials at a time go through shared memory, and a
 // thread's partial loads are independent of one another, so the merge costs
 // a few L2 round trips.
-constexpr int kMergeMaxThreads = 256;   // >= 8 heads x 128 / 4 columns
+constexpr int kMergeMaxThreads = 512;   // >= 16 rows x 128 / 4 columns
+constexpr int kMergeRows = 16;          // query rows of a pair at most
 constexpr int kMergeChunk = 64;
 constexpr int kMergeDirect = 8;      // up to this many partials: no staging
 
@@ -1160,9 +1170,9 @@ inline int merge_threads(int G, int D) { return (G * D / 4 + 31) / 32 * 32; }
 // Small CTAs with few registers, so that they fit beside the split kernel's
 // CTAs and start (programmatic dependent launch) before it drains.
 template <int D>
-__global__ void __launch_bounds__(kMergeMaxThreads, 4) paged_decode_merge_kernel(const MergeParams p)
+__global__ void __launch_bounds__(kMergeMaxThreads, 2) paged_decode_merge_kernel(const MergeParams p)
 {
-    __shared__ float2 sml[kMergeChunk * 8];
+    __shared__ float2 sml[kMergeChunk * kMergeRows];
     // the next kernel may start only once the split kernel (and with it the
     // step's appends to the cache) is complete: a following call that reads
     // its inputs early sees them
@@ -1262,12 +1272,12 @@ __global__ void __launch_bounds__(kMergeMaxThreads, 4) paged_decode_merge_kernel
                                     : (size_t)(cslot0 + (k - na)) * p.prow + crow + gg;
             float2 v = __ldcg(&p.part_ml[r]);
             if (!(v.y > 0.f)) v = make_float2(-INFINITY, 0.f);     // empty partial
-            sml[kk * 8 + gg] = v;
+            sml[kk * kMergeRows + gg] = v;
         }
         __syncthreads();
         if (!live) continue;
         float cm = -INFINITY;
-        for (int k = 0; k < nk; ++k) cm = fmaxf(cm, sml[k * 8 + g].x);
+        for (int k = 0; k < nk; ++k) cm = fmaxf(cm, sml[k * kMergeRows + g].x);
         const float Mn = fmaxf(M, cm);
         const float r = Mn == -INFINITY ? 0.f : exp2f(M - Mn);
         den *= r;
@@ -1279,7 +1289,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads, 4) paged_decode_merge_kernel
             const size_t prw = k < na ? (size_t)(aslot0 + k) * p.prow + g
                                       : (size_t)(cslot0 + (k - na)) * p.prow + crow + g;
             const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + prw * D) + d4);
-            const float2 v = sml[kk * 8 + g];
+            const float2 v = sml[kk * kMergeRows + g];
             const float f = v.y > 0.f ? exp2f(v.x - M) : 0.f;
             den += f * v.y;
             acc.x += f * o.x;
@@ -1416,8 +1426,9 @@ struct WsLayout {
 };
 
 // Partial slots: one per (stream, KV head) plus one per warp (a warp's
-// partial of pair x goes to slot x + w).  nr == 2 (prefix chunks) gives
-// slots of KV_PREFIX_MAX_ROWS rows, otherwise G rows.
+// partial of pair x goes to slot x + w).  nr == 2 (prefix chunks, or groups
+// of 9-16 rows) gives slots of KV_PREFIX_MAX_ROWS rows, otherwise G rows.
+// Hkv is the number of (virtual) KV heads the kernels iterate over.
 WsLayout ws_layout(int B, int nc, int Hq, int Hkv, int D, int warps_total, int nr)
 {
     const int prow = nr == 2 ? KV_PREFIX_MAX_ROWS : Hq / Hkv;
@@ -1431,14 +1442,59 @@ WsLayout ws_layout(int B, int nc, int Hq, int Hkv, int D, int warps_total, int n
     return L;
 }
 
+// Query heads per KV head, G = Hq / Hkv: up to 8 rows run the kernel with one
+// row tile of state, 9-16 the one with two; a larger G (MQA on a many-head
+// model) is served as 2^k virtual KV heads of G / 2^k <= 16 rows each, which
+// read the same cache tiles (warps at the same point of neighbouring virtual
+// heads run side by side, so the repeats mostly hit L2).
+struct HeadSplit {
+    int Hkv_v, G_v, hshift;
+};
+
+int head_split(int Hq, int Hkv, HeadSplit& hs)
+{
+    const int G = Hq / Hkv;
+    int k = 0;
+    while ((G >> k) > KV_PREFIX_MAX_ROWS) ++k;
+    if (k > 3 || G % (1 << k) != 0) return KV_ERR_UNSUPPORTED;    // G <= 128, even split
+    hs.hshift = k;
+    hs.G_v = G >> k;
+    hs.Hkv_v = Hkv << k;
+    return KV_OK;
+}
+
 int check_shape(int num_seqs, int Hq, int Hkv, int D, int kv_dtype)
 {
     if (num_seqs < 0 || Hq <= 0 || Hkv <= 0) return KV_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return KV_ERR_INVALID_ARG;
-    const int G = Hq / Hkv;
-    if (G > 8) return KV_ERR_UNSUPPORTED;
+    HeadSplit hs;
+    if (int rc = head_split(Hq, Hkv, hs)) return rc;
     if (D != 64 && D != 128) return KV_ERR_UNSUPPORTED;
     if (kv_dtype != KV_DTYPE_BF16 && kv_dtype != KV_DTYPE_FP8_E4M3) return KV_ERR_UNSUPPORTED;
+    return KV_OK;
+}
+
+// Everything about a launch that the workspace size depends on: the head
+// split, the kernel (row tiles nr), the persistent grid and the partial
+// slots (a second set of per-warp slots for the prefix-chunk phase).
+struct LaunchPlan {
+    HeadSplit hs;
+    int nr, grid, warps_total, slot_warps;
+    WsLayout ws;
+};
+
+int plan_launch(int B, int nc, int Hq, int Hkv, int D, bool fp8, LaunchPlan& lp)
+{
+    if (int rc = head_split(Hq, Hkv, lp.hs)) return rc;
+    // prefix chunks pack at least two members' rows into 16: G <= 8
+    if (nc > 0 && 2 * (Hq / Hkv) > KV_PREFIX_MAX_ROWS) return KV_ERR_UNSUPPORTED;
+    lp.nr = (nc > 0 || lp.hs.G_v > 8) ? 2 : 1;
+    int sms = 0, cps = 0;
+    if (int rc = device_info(D, fp8, lp.nr, sms, cps)) return rc;
+    lp.grid = sms * cps;
+    lp.warps_total = lp.grid * kWarps;
+    lp.slot_warps = nc > 0 ? 2 * lp.warps_total : lp.warps_total;
+    lp.ws = ws_layout(B, nc, Hq, lp.hs.Hkv_v, D, lp.slot_warps, lp.nr);
     return KV_OK;
 }
 
@@ -1513,25 +1569,27 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     const int nc = pre ? pre->nc : 0;
     if (nc < 0 || nc > num_seqs / 2) return KV_ERR_INVALID_ARG;
     if (nc > 0 && (!pre->chunk || !pre->seq_chunk)) return KV_ERR_INVALID_ARG;
-    const int nr = nc > 0 ? 2 : 1;
     const bool fp8 = kv_dtype == KV_DTYPE_FP8_E4M3;
     if (fp8 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
         return KV_ERR_INVALID_ARG;
+    HeadSplit hs0;
+    if (int rc = head_split(num_q_heads, num_kv_heads, hs0)) return rc;
     // flat work indices and tensor-map rows must fit in int32
-    if (((long long)num_seqs + nc) * max_blocks_per_seq * num_kv_heads >= INT_MAX ||
+    if (((long long)num_seqs + nc) * max_blocks_per_seq * hs0.Hkv_v >= INT_MAX ||
         (long long)num_blocks * num_kv_heads >= INT_MAX ||
         (long long)max_blocks_per_seq * kBlock >= INT_MAX)
         return KV_ERR_UNSUPPORTED;
 
-    // one launch: the 16-row kernel (prefix chunks, then sequences) or the
-    // plain one; with chunks each phase has its own partial slots
-    int sms = 0, cps = 0;
-    if (int rc = device_info(head_dim, fp8, nr, sms, cps)) return rc;
-    const int grid = sms * cps;
-    const int warps_total = grid * kWarps;
-    const int slot_warps = nr == 2 ? 2 * warps_total : warps_total;
-    const WsLayout ws =
-        ws_layout(num_seqs, nc, num_q_heads, num_kv_heads, head_dim, slot_warps, nr);
+    // one launch: the 16-row kernel (prefix chunks, then sequences; or
+    // groups of 9-16 rows) or the plain one; with chunks each phase has its
+    // own partial slots
+    LaunchPlan lp;
+    if (int rc = plan_launch(num_seqs, nc, num_q_heads, num_kv_heads, head_dim, fp8, lp))
+        return rc;
+    const int nr = lp.nr, grid = lp.grid, warps_total = lp.warps_total;
+    const int slot_warps = lp.slot_warps;
+    const int Hkv_v = lp.hs.Hkv_v;
+    const WsLayout ws = lp.ws;
     if (workspace_bytes < ws.total) return KV_ERR_INVALID_ARG;
 
     CUtensorMap mk, mv;
@@ -1553,8 +1611,9 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.v_cache = app ? static_cast<uint8_t*>(app->v_cache) : nullptr;
     dp.B = num_seqs;
     dp.Hq = num_q_heads;
-    dp.Hkv = num_kv_heads;
-    dp.G = num_q_heads / num_kv_heads;
+    dp.Hkv = Hkv_v;
+    dp.G = lp.hs.G_v;
+    dp.hshift = lp.hs.hshift;
     dp.max_blocks = max_blocks_per_seq;
     dp.num_blocks = num_blocks;
     dp.warps_total = warps_total;
@@ -1569,7 +1628,7 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.seq_chunk = nc > 0 ? pre->seq_chunk : nullptr;
     dp.nc = nc;
     dp.prow = nr == 2 ? KV_PREFIX_MAX_ROWS : dp.G;
-    dp.slot_base = nr == 2 ? warps_total : 0;
+    dp.slot_base = nc > 0 ? warps_total : 0;
     dp.early = pre && (pre->flags & KV_DECODE_EARLY_INPUTS) ? 1 : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1598,12 +1657,12 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     mp.prow = dp.prow;
     mp.B = num_seqs;
     mp.Hq = num_q_heads;
-    mp.Hkv = num_kv_heads;
+    mp.Hkv = Hkv_v;
     mp.G = dp.G;
     mp.max_blocks = max_blocks_per_seq;
-    mp.nslots = (num_seqs + nc) * num_kv_heads + slot_warps;
+    mp.nslots = (num_seqs + nc) * Hkv_v + slot_warps;
     mp.out_f32 = dp.out_f32;
-    const unsigned mgrid = (unsigned)(num_seqs * num_kv_heads);
+    const unsigned mgrid = (unsigned)(num_seqs * Hkv_v);
     const unsigned mthreads = (unsigned)merge_threads(dp.G, head_dim);
     err = head_dim == 128
               ? launch_pdl(paged_decode_merge_kernel<128>, mgrid, mthreads, 0, st, mp)
@@ -1678,10 +1737,11 @@ extern "C" int paged_decode_workspace_bytes(int num_seqs, int num_q_heads, int n
     if (!bytes) return KV_ERR_INVALID_ARG;
     *bytes = 0;
     if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
-    int sms = 0, cps = 0;
-    if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, 1, sms, cps)) return rc;
-    *bytes = ws_layout(num_seqs, 0, num_q_heads, num_kv_heads, head_dim, sms * cps * kWarps, 1)
-                 .total;
+    LaunchPlan lp;
+    if (int rc = plan_launch(num_seqs, 0, num_q_heads, num_kv_heads, head_dim,
+                             kv_dtype == KV_DTYPE_FP8_E4M3, lp))
+        return rc;
+    *bytes = lp.ws.total;
     return KV_OK;
 }
 
@@ -1693,12 +1753,11 @@ extern "C" int paged_decode_prefix_workspace_bytes(int num_seqs, int num_chunks,
     *bytes = 0;
     if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
     if (num_chunks < 0 || num_chunks > num_seqs / 2) return KV_ERR_INVALID_ARG;
-    const int nr = num_chunks > 0 ? 2 : 1;
-    int sms = 0, cps = 0;
-    if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, nr, sms, cps)) return rc;
-    *bytes = ws_layout(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
-                       sms * cps * kWarps * nr, nr)
-                 .total;
+    LaunchPlan lp;
+    if (int rc = plan_launch(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
+                             kv_dtype == KV_DTYPE_FP8_E4M3, lp))
+        return rc;
+    *bytes = lp.ws.total;
     return KV_OK;
 }
 

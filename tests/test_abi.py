@@ -91,8 +91,14 @@ def test_gpu_entry_points_reject_bad_arguments_without_a_gpu(lib_path):
         pk.KV_ERR_UNSUPPORTED
     assert L.paged_decode_attention(None, 0, None, None, None, 0, 1.0, 1.0, 1, None, 1, None,
                                     1, 32, 8, 96, 0.1, None, 0, None) == pk.KV_ERR_UNSUPPORTED
-    assert L.paged_decode_attention(None, 0, None, None, None, 0, 1.0, 1.0, 1, None, 1, None,
-                                    1, 48, 3, 128, 0.1, None, 0, None) == pk.KV_ERR_UNSUPPORTED
+    # group sizes: 17 and 34 have no even split into sub-groups of <= 16 rows,
+    # 256 exceeds the largest split; 16, 24 and 128 pass the shape checks
+    # (and then fail on the NULL buffers, still before any CUDA call)
+    for hq, hkv, want in ((51, 3, pk.KV_ERR_UNSUPPORTED), (68, 2, pk.KV_ERR_UNSUPPORTED),
+                          (256, 1, pk.KV_ERR_UNSUPPORTED), (48, 3, pk.KV_ERR_INVALID_ARG),
+                          (48, 2, pk.KV_ERR_INVALID_ARG), (128, 1, pk.KV_ERR_INVALID_ARG)):
+        assert L.paged_decode_attention(None, 0, None, None, None, 0, 1.0, 1.0, 1, None, 1, None,
+                                        1, hq, hkv, 128, 0.1, None, 0, None) == want, (hq, hkv)
     assert L.paged_decode_attention(None, 0, None, None, None, 0, 1.0, 1.0, 1, None, 1, None,
                                     1, 30, 8, 128, 0.1, None, 0, None) == pk.KV_ERR_INVALID_ARG
     assert L.paged_decode_attention(None, 0, None, None, None, 0, 1.0, 1.0, 1, None, 1, None,

@@ -191,6 +191,52 @@ def test_one_pair_split_over_hundreds_of_warps(lens, kv_dtype):
     check_case(case, what="fused early", fused=True, early_inputs=True)
 
 
+LARGE_GROUP_LENS = [1, 17, 300, 4097, 2000, 33]
+
+
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+@pytest.mark.parametrize("Hq,Hkv,D", [(12, 1, 128), (16, 2, 128), (24, 3, 128), (32, 1, 128),
+                                      (48, 2, 64), (64, 1, 128), (128, 1, 64)])
+def test_large_query_groups(Hq, Hkv, D, kv_dtype):
+    """G = 12..128, MQA on many-head models ("KV cache complete guide",
+    section "(2) GQA": one KV head for all query heads): 9-16 rows run the
+    two-row-tile kernel, larger groups run as 2, 4 or 8 sub-groups that read
+    the same KV tiles.  Two-launch and fused paths, float32 output, and the
+    append written by every sub-group lands once, bit-exact."""
+    case = workloads.make_custom(len(LARGE_GROUP_LENS), Hq, Hkv, D, LARGE_GROUP_LENS,
+                                 kv_dtype=kv_dtype, seed=Hq + Hkv)
+    what = "Hq%d Hkv%d D%d dt%d" % (Hq, Hkv, D, kv_dtype)
+    check_case(case, what=what)
+    check_case(case, what="fused early " + what, fused=True, early_inputs=True)
+    check_case(case, what="f32 " + what, out_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("Hq", [32, 64])
+def test_mqa_full_size_and_deterministic(Hq):
+    """One KV head for Hq query heads at the 8B layer's batch and context
+    (32 sequences x 8193 tokens, d128): every output against the oracle, and
+    two runs bit-identical."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(32, Hq, 1, 128, [8193] * 32, seed=Hq)
+    out1 = check_case(case, what="MQA %d" % Hq, fused=True, early_inputs=True)
+    assert out1 < 2e-3
+    o1, _, _ = H.gpu_step(case, fused=True, early_inputs=True)
+    o2, _, _ = H.gpu_step(case, fused=True, early_inputs=True)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert pk.get_device_error()[0] == 0
+
+
+def test_prefix_chunks_refuse_groups_above_eight():
+    """A chunk packs at least two members' rows into 16: G > 8 has no chunks,
+    and the shared-prefix call refuses a chunk table for it."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(4, 32, 2, 128, [100, 100, 100, 100], seed=3)
+    with pytest.raises(pk.KVError):
+        pk.prefix_chunks(case.block_tables, case.context_lens, 16)
+    with pytest.raises(pk.KVError):
+        pk.prefix_workspace_bytes(4, 1, 32, 2, 128)
+
+
 def test_group_sizes_two_three_five_seven():
     for G in (2, 3, 5, 7):
         case = workloads.make_custom(3, 3 * G, 3, 128, [40, 700, 2000], seed=G)
