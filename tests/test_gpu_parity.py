@@ -243,19 +243,22 @@ def test_group_sizes_two_three_five_seven():
         check_case(case, what="G=%d" % G)
 
 
-def test_many_sequences_beyond_register_scan():
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 1)])
+def test_many_sequences_beyond_register_scan(Hq, Hkv):
     # more than 256 sequences takes the second scan path of the split kernel
-    # (three chunks of 256 here), with some empty contexts mixed in
+    # (three chunks of 256 here), with some empty contexts mixed in; 32q/1kv
+    # runs as two 16-row sub-groups per KV head
     lens = (np.arange(700) * 37) % 500 + 1
-    case = workloads.make_custom(700, 8, 2, 64, lens, seed=77)
+    case = workloads.make_custom(700, Hq, Hkv, 64, lens, seed=77)
     case.context_lens[::97] = 0
-    check_case(case, what="B=700")
+    check_case(case, what="B=700 G=%d" % (Hq // Hkv))
     check_case(case, what="B=700 fused", fused=True)
 
 
-def test_empty_contexts_give_zeros():
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 1), (64, 2)])
+def test_empty_contexts_give_zeros(Hq, Hkv):
     lens = [0, 33, 0, 1, 0]
-    case = workloads.make_custom(5, 8, 2, 128, [max(x, 1) for x in lens], seed=4)
+    case = workloads.make_custom(5, Hq, Hkv, 128, [max(x, 1) for x in lens], seed=4)
     case.context_lens = np.array(lens, dtype=np.int32)
     err = check_case(case, what="empty contexts")
     out, _, _ = H.gpu_step(case)
@@ -266,8 +269,9 @@ def test_empty_contexts_give_zeros():
     assert err < 2e-3
 
 
-def test_nan_canaries_in_unused_slots_are_never_read():
-    case = workloads.make_custom(4, 16, 4, 128, [1, 18, 333, 1000], seed=8, slack=0.5)
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (48, 1)])
+def test_nan_canaries_in_unused_slots_are_never_read(Hq, Hkv):
+    case = workloads.make_custom(4, Hq, Hkv, 128, [1, 18, 333, 1000], seed=8, slack=0.5)
     used = np.zeros(case.num_blocks * 16, dtype=bool)
     for s, L in enumerate(case.context_lens):
         for pos in range(int(L)):
