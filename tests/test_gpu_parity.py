@@ -260,7 +260,9 @@ def test_empty_contexts_give_zeros(Hq, Hkv):
     lens = [0, 33, 0, 1, 0]
     case = workloads.make_custom(5, Hq, Hkv, 128, [max(x, 1) for x in lens], seed=4)
     case.context_lens = np.array(lens, dtype=np.int32)
-    err = check_case(case, what="empty contexts")
+    check_case(case, what="empty contexts")
+    # the tolerance without the bf16 output rounding: float32 output
+    err = check_case(case, what="empty contexts f32", out_dtype=torch.float32)
     out, _, _ = H.gpu_step(case)
     out_np = out.float().cpu().numpy()
     for s_, L in enumerate(lens):
