@@ -139,6 +139,8 @@ struct DecodeParams {
     int warps_total;
     int min_q1;              // minimum range of a warp in the sequence phase
     int hshift;              // a KV head serves 1 << hshift virtual heads of G rows
+    int Hkv_p;               // physical KV heads (Hkv >> hshift)
+    int team_slots;          // partial slots of one team: streams * Hkv_p + its warps
     float sl2;               // scale * log2(e) (* k_scale)
     float v_scale;
     float k_qscale, v_qscale;    // quantisation scales of the fused append (E4M3)
@@ -243,6 +245,21 @@ __device__ __forceinline__ int prefix_of(const int32_t* chunk, const int32_t* se
     return P;
 }
 
+// Sub-groups of a KV head exist only in the two-row-tile kernel (a group
+// above 16 rows leaves sub-groups of 9-16 rows), so the one-row-tile kernel
+// folds them away at compile time.
+template <int NR>
+__device__ __forceinline__ int hshift_of(const DecodeParams& p)
+{
+    return NR == 2 ? p.hshift : 0;
+}
+
+template <int NR>
+__device__ __forceinline__ int hkv_phys(const DecodeParams& p)
+{
+    return NR == 2 ? p.Hkv_p : p.Hkv;
+}
+
 template <int NR>
 __device__ __forceinline__ Stream stream_at(const DecodeParams& p, int sigma)
 {
@@ -293,7 +310,7 @@ __device__ __forceinline__ void fill_window(Win& e, const DecodeParams& p, int n
     while (r >= S.nblk - j) {
         r -= S.nblk - j;
         j = 0;
-        if (++h == p.Hkv) {
+        if (++h == hkv_phys<NR>(p)) {
             h = 0;
             do {
                 if (++sg >= ns) return;      // inconsistent input: leave the entry invalid
@@ -694,12 +711,18 @@ struct Seg {
 // the rest.  Only plain stores: a stream switch in mid-range does not stall
 // the warp's pipeline.
 template <int D, bool FP8, int NR>
-__device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, int b0,
+__device__ __forceinline__ void finalize(const DecodeParams& p, int wl, int q, int b0,
                                          int slot_base, const Seg& sg,
                                          const float (&m)[NR], const float (&l)[NR],
                                          const float (&o)[NR][D / 16][4], int lane)
 {
     const int g = lane >> 2, t = lane & 3;
+    // this warp's partial slot: each team (sub-group) has its own run of
+    // slots, in which pair x's partial of the team's warp wl goes to x + wl
+    const int hsh = hshift_of<NR>(p);
+    const int team = sg.pair & ((1 << hsh) - 1);
+    const size_t slot = (size_t)slot_base + (size_t)team * p.team_slots +
+                        (size_t)(sg.pair >> hsh) + wl;
     float la[NR], lb[NR], ma[NR], mb[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -739,7 +762,6 @@ __device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, in
             }
         }
     } else {
-        const size_t slot = (size_t)slot_base + sg.pair + w;
         float* po = p.part_o + slot * p.prow * D;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
@@ -766,7 +788,7 @@ __device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, in
         // [flat_first, flat_first + (end - base))
         const int flat_first = b0 + sg.i0;
         const int w_last = (flat_first + (sg.end - sg.base) - 1) / q;
-        p.pair_meta[sg.pair] = make_int4(slot_base + sg.pair + w, w_last - w + 1, sg.cj, 0);
+        p.pair_meta[sg.pair] = make_int4((int)slot, w_last - wl + 1, sg.cj, 0);
     }
 }
 
@@ -774,7 +796,7 @@ __device__ __forceinline__ void finalize(const DecodeParams& p, int w, int q, in
 // i.e. row (L-1) % 16 of the pair's last block `id`.  Writes the cache in
 // global memory and the same bytes into this warp's copy of the tile in
 // shared memory (which the bulk copy may have filled before the write).
-template <int D, bool FP8>
+template <int D, bool FP8, int NR>
 __device__ __forceinline__ void append_patch(const DecodeParams& p, int s, int h, int id, int L,
                                              uint32_t kst, uint32_t vst, int lane)
 {
@@ -785,7 +807,7 @@ __device__ __forceinline__ void append_patch(const DecodeParams& p, int s, int h
         const int c = isv ? lane - CH : lane;
         const int r = (L - 1) & (kBlock - 1);
         // cache and new tokens are indexed by the physical KV head
-        const int Hp = p.Hkv >> p.hshift, hp = h >> p.hshift;
+        const int Hp = hkv_phys<NR>(p), hp = h >> hshift_of<NR>(p);
         const size_t src = ((size_t)s * Hp + hp) * D + 8 * c;
         const size_t dst = (((size_t)id * Hp + hp) * kBlock + r) * D + 8 * c;
         const uint4 x = __ldg(reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src));
@@ -812,6 +834,14 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
     extern __shared__ uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int w = blockIdx.x * kWarps + warp;
+    // Groups cut into 2^hshift sub-groups: the warps form one team per
+    // sub-group, and every team partitions the same (sequence, KV head,
+    // block) units the same way, so the warps of all teams that read a tile
+    // do so at about the same time and the repeats hit L2.
+    const int hsh = hshift_of<NR>(p), Hkv_p = hkv_phys<NR>(p);
+    const int Wt = p.warps_total >> hsh;
+    const int team = w / Wt, wl = w - team * Wt;
+    if (team >= (1 << hsh)) return;
 
     const uint32_t sraw = smem_u32(smem_raw);
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
@@ -867,7 +897,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            incl[u] = warp_incl_scan(nbv[u] * p.Hkv, lane) + carry;
+            incl[u] = warp_incl_scan(nbv[u] * Hkv_p, lane) + carry;
             carry = __shfl_sync(kFull, incl[u], 31);
         }
         int total = carry;
@@ -882,14 +912,14 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
             int sum = 0;
 #pragma unroll
             for (int u = 0; u < U; ++u) sum += v[u];
-            total += warp_sum(sum) * p.Hkv;
+            total += warp_sum(sum) * Hkv_p;
         }
         if (total == 0) continue;
-        int q = (total + p.warps_total - 1) / p.warps_total;
+        int q = (total + Wt - 1) / Wt;
         if (q < min_q) q = min_q;
         const int weff = (total + q - 1) / q;
-        if (w >= weff) continue;
-        const int b0 = w * q;
+        if (wl >= weff) continue;
+        const int b0 = wl * q;
         const int cnt = min(q, total - b0);
 
         // ---- 2. the (stream, head, block) where the range starts ----------------
@@ -900,7 +930,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
             if (s0 < 0 && mball) {
                 const int src = __ffs(mball) - 1;
                 s0 = s_lo + u * 32 + src;
-                excl = __shfl_sync(kFull, incl[u] - nbv[u] * p.Hkv, src);
+                excl = __shfl_sync(kFull, incl[u] - nbv[u] * Hkv_p, src);
             }
         }
         if (s0 < 0) {
@@ -910,7 +940,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int sg = base + u * 32 + lane;
-                    v[u] = sg < ns ? max(stream_at<NR>(p, sg).nblk, 0) * p.Hkv : 0;
+                    v[u] = sg < ns ? max(stream_at<NR>(p, sg).nblk, 0) * Hkv_p : 0;
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -966,14 +996,14 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
             const int L = __shfl_sync(kFull, cur.L, src);
             if (lane == 0) {
                 const bool valid = id >= 0 && id < p.num_blocks;
-                const int pair = s * p.Hkv + h;
+                const int pair = s * p.Hkv + (h << hsh) + team;
                 meta[sst] = make_int4(valid ? pair : -1 - pair, blk, L, id);
                 const uint32_t bar = bar0 + sst * 8;
                 const uint32_t dst = stage0 + (uint32_t)(sst * G::STAGE);
                 if (valid) {
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(bar, (uint32_t)G::STAGE);
-                    const int z = id * (p.Hkv >> p.hshift) + (h >> p.hshift);
+                    const int z = id * Hkv_p + h;
                     // KV tiles are read once per step: keep them from evicting
                     // the block tables, queries and partials from L2
                     const uint64_t pol = l2_evict_first_policy();
@@ -1041,7 +1071,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
             const int pair = valid ? mt.x : -1 - mt.x;
             const int blk = mt.y, L = mt.z;
             if (pair != sg.pair) {
-                if (open) finalize<D, FP8, NR>(p, w, q, b0, slot_base, sg, m, l, o, lane);
+                if (open) finalize<D, FP8, NR>(p, wl, q, b0, slot_base, sg, m, l, o, lane);
                 open = true;
                 const int sig = pair / p.Hkv;
                 const Stream S = stream_at<NR>(p, sig);
@@ -1085,7 +1115,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                 const int rest = L - (blk + 1) * kBlock;
                 const int nvalid = min(kBlock, rest);
                 if (own_last && nvalid == rest)
-                    append_patch<D, FP8>(p, sg.s, sg.h, id2, L, kb2, kb2 + G::TILE, lane);
+                    append_patch<D, FP8, NR>(p, sg.s, sg.h, id2, L, kb2, kb2 + G::TILE, lane);
                 const uint32_t kbs[2] = {kb, kb2};
                 attend<D, FP8, 2, NR>(sg.nr, kbs, nvalid, qf, p.sl2, m, l, o, lane);
                 sg.last = blk + 1;
@@ -1100,7 +1130,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                 if (valid) {
                     const int nvalid = min(kBlock, L - blk * kBlock);
                     if (own_last && nvalid == L - blk * kBlock)
-                        append_patch<D, FP8>(p, sg.s, sg.h, mt.w, L, kb, kb + G::TILE, lane);
+                        append_patch<D, FP8, NR>(p, sg.s, sg.h, mt.w, L, kb, kb + G::TILE, lane);
                     const uint32_t kbs[1] = {kb};
                     attend<D, FP8, 1, NR>(sg.nr, kbs, nvalid, qf, p.sl2, m, l, o, lane);
                 }
@@ -1111,7 +1141,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                 i += 1;
             }
         }
-        if (open) finalize<D, FP8, NR>(p, w, q, b0, slot_base, sg, m, l, o, lane);
+        if (open) finalize<D, FP8, NR>(p, wl, q, b0, slot_base, sg, m, l, o, lane);
     }
 }
 
@@ -1444,9 +1474,10 @@ WsLayout ws_layout(int B, int nc, int Hq, int Hkv, int D, int warps_total, int n
 
 // Query heads per KV head, G = Hq / Hkv: up to 8 rows run the kernel with one
 // row tile of state, 9-16 the one with two; a larger G (MQA on a many-head
-// model) is served as 2^k virtual KV heads of G / 2^k <= 16 rows each, which
-// read the same cache tiles (warps at the same point of neighbouring virtual
-// heads run side by side, so the repeats mostly hit L2).
+// model) is served as 2^k virtual KV heads of G / 2^k <= 16 rows each.  The
+// split kernel's warps then form 2^k teams, one per sub-group, that cut the
+// same units the same way, so a tile's 2^k reads come at about the same
+// time and all but the first hit L2.
 struct HeadSplit {
     int Hkv_v, G_v, hshift;
 };
@@ -1614,6 +1645,8 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.Hkv = Hkv_v;
     dp.G = lp.hs.G_v;
     dp.hshift = lp.hs.hshift;
+    dp.Hkv_p = num_kv_heads;
+    dp.team_slots = (num_seqs + nc) * num_kv_heads + (warps_total >> lp.hs.hshift);
     dp.max_blocks = max_blocks_per_seq;
     dp.num_blocks = num_blocks;
     dp.warps_total = warps_total;
