@@ -43,6 +43,10 @@
 //    fused in: the warp that owns a pair's last block writes the new K/V to
 //    the cache and patches its own copy of that tile in shared memory before
 //    using it.
+//  * Query groups of 9-16 rows fill both 8-row halves of the MMA tile (the
+//    two-row-tile kernel); larger groups (MQA on many-head models) run as
+//    2^k sub-groups of <= 16 rows, one team of warps each, the teams cutting
+//    the same units the same way so that a tile's repeated reads hit L2.
 //  * Shared prefixes (paged_decode with a chunk table): sequences whose
 //    block tables start with the same blocks ("KV cache complete guide",
 //    sections "(3) Prefix Caching" and "(4) PagedAttention") are cut into
