@@ -268,7 +268,10 @@ def run_reference(args):
               "KV), float64 C oracle with OpenMP" % (spec["B"], case.Hkv,
                                                      int(case.context_lens[0]),
                                                      case.logical_kv_bytes()))
-    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 0,
+    # n_gpus is the launch's N, as in our arm's line; the oracle itself uses
+    # the host cores of rank 0 and no GPU
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": max(world, args.gpus), "gpu_used": False,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(args.config, args.batch),
