@@ -109,6 +109,29 @@ for _name, (_res, _args) in _SIGS.items():
     _fn.restype = _res
     _fn.argtypes = _args
 
+# The per-step calls go through the CPython-API module _pkvfast when it was
+# built (plain integers and floats, no ctypes marshalling); it links the same
+# libpagedkv.so, which the dynamic loader shares with the ctypes handle above.
+try:
+    from . import _pkvfast as _fast
+except ImportError:
+    _fast = None
+
+
+def _hot(name):
+    return getattr(_fast, name) if _fast is not None else getattr(_lib, name)
+
+
+_HOT_PAGED_DECODE = _hot("paged_decode")
+_HOT_PAGED_DECODE_STEP = _hot("paged_decode_step")
+_HOT_PAGED_DECODE_ATTENTION = _hot("paged_decode_attention")
+_HOT_KV_APPEND = _hot("kv_append")
+
+
+def fast_path():
+    """True when the per-step calls bypass ctypes (module _pkvfast)."""
+    return _fast is not None
+
 
 def native_library_path():
     return _LIB_PATH
@@ -137,6 +160,13 @@ def _stream_ptr(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _stream_int(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
 
 
 def _cache_dtype(t):
@@ -295,9 +325,9 @@ def kv_append(k, v, k_cache, v_cache, slot_mapping, k_scale=1.0, v_scale=1.0, st
     device) into the caches ([NB, Hkv, 16, D], bfloat16 or uint8 E4M3)."""
     T, Hkv, D = k.shape
     NB = k_cache.shape[0]
-    _check(_lib.kv_append(_dptr(k), _dptr(v), _dptr(k_cache), _dptr(v_cache),
-                          _dptr(slot_mapping), T, Hkv, D, NB, _cache_dtype(k_cache),
-                          float(k_scale), float(v_scale), _stream_ptr(stream)), "kv_append")
+    _check(_HOT_KV_APPEND(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          slot_mapping.data_ptr(), T, Hkv, D, NB, _cache_dtype(k_cache),
+                          float(k_scale), float(v_scale), _stream_int(stream)), "kv_append")
 
 
 def kv_copy_blocks(k_cache, v_cache, src, dst, stream=None):
@@ -333,11 +363,11 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
     NB, Hkv, _, D2 = k_cache.shape
     assert D == D2
     out_dtype = F32 if out.dtype == torch.float32 else BF16
-    _check(_lib.paged_decode_attention(
-        _dptr(out), out_dtype, _dptr(q), _dptr(k_cache), _dptr(v_cache), _cache_dtype(k_cache),
-        float(k_scale), float(v_scale), NB, _dptr(block_tables), block_tables.shape[1],
-        _dptr(context_lens), B, Hq, Hkv, D, float(scale), _dptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+    _check(_HOT_PAGED_DECODE_ATTENTION(
+        out.data_ptr(), out_dtype, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        _cache_dtype(k_cache), float(k_scale), float(v_scale), NB, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, D, float(scale),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_int(stream)),
         "paged_decode_attention")
 
 
@@ -369,12 +399,12 @@ def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, cont
     B, Hq, D = q.shape
     NB, Hkv, _, _ = k_cache.shape
     out_dtype = F32 if out.dtype == torch.float32 else BF16
-    _check(_lib.paged_decode_step(
-        _dptr(out), out_dtype, _dptr(q), _dptr(k_new), _dptr(v_new), _dptr(k_cache),
-        _dptr(v_cache), _cache_dtype(k_cache), float(k_scale), float(v_scale), NB,
-        _dptr(block_tables), block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D,
-        float(scale), _dptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream_ptr(stream)), "paged_decode_step")
+    _check(_HOT_PAGED_DECODE_STEP(
+        out.data_ptr(), out_dtype, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), _cache_dtype(k_cache), float(k_scale),
+        float(v_scale), NB, block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), B, Hq, Hkv, D, float(scale), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_int(stream)), "paged_decode_step")
 
 
 PREFIX_CHUNK_INTS = 18      # KV_PREFIX_CHUNK_INTS
@@ -435,16 +465,14 @@ def paged_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, wo
     NB, Hkv, _, _ = k_cache.shape
     out_dtype = F32 if out.dtype == torch.float32 else BF16
     nc = int(chunks.shape[0]) if chunks is not None else 0
-    null = ctypes.c_void_p(0)
-    _check(_lib.paged_decode(
-        _dptr(out), out_dtype, _dptr(q), _dptr(k_new) if k_new is not None else null,
-        _dptr(v_new) if v_new is not None else null, _dptr(k_cache), _dptr(v_cache),
-        _cache_dtype(k_cache), float(k_scale), float(v_scale), NB, _dptr(block_tables),
-        block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D, float(scale),
-        _dptr(chunks) if nc else null, _dptr(seq_chunk) if nc else null, nc,
-        DECODE_EARLY_INPUTS if early_inputs else 0, _dptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
-        "paged_decode")
+    _check(_HOT_PAGED_DECODE(
+        out.data_ptr(), out_dtype, q.data_ptr(), k_new.data_ptr() if k_new is not None else 0,
+        v_new.data_ptr() if v_new is not None else 0, k_cache.data_ptr(), v_cache.data_ptr(),
+        _cache_dtype(k_cache), float(k_scale), float(v_scale), NB, block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), B, Hq, Hkv, D, float(scale),
+        chunks.data_ptr() if nc else 0, seq_chunk.data_ptr() if nc else 0, nc,
+        DECODE_EARLY_INPUTS if early_inputs else 0, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_int(stream)), "paged_decode")
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -81,7 +81,33 @@ def build(force=False, verbose_ptxas=False, jobs=None):
         if r.returncode != 0:
             raise RuntimeError("link failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
         os.replace(tmp, LIB)
+    build_fast(force=force)
     return LIB
+
+
+PYEXT_SRC = os.path.join(PKG, "pyext", "pkvfast.c")
+
+
+def build_fast(force=False):
+    """Compile the CPython-API module ``_pkvfast`` (the per-step calls without
+    ctypes marshalling) against ``libpagedkv.so``; returns its path, or None
+    where this Python has no headers (the ctypes binding then serves every
+    call)."""
+    import sysconfig
+    inc = sysconfig.get_paths().get("include")
+    if not inc or not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    out = os.path.join(PKG, "_pkvfast" + sysconfig.get_config_var("EXT_SUFFIX"))
+    if not force and not _stale(out, [PYEXT_SRC, LIB, __file__] + _headers()):
+        return out
+    tmp = out + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-shared", "-fPIC", "-Wall", "-Wextra", "-I", inc, "-I", INCLUDE,
+           PYEXT_SRC, "-o", tmp, "-L", PKG, "-l:libpagedkv.so", "-Wl,-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("compile failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

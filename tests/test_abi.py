@@ -103,3 +103,22 @@ def test_gpu_entry_points_reject_bad_arguments_without_a_gpu(lib_path):
                                     1, 30, 8, 128, 0.1, None, 0, None) == pk.KV_ERR_INVALID_ARG
     assert L.paged_decode_attention(None, 0, None, None, None, 0, 1.0, 1.0, 1, None, 1, None,
                                     0, 32, 8, 128, 0.1, None, 0, None) == pk.KV_OK
+
+
+def test_fast_call_module_marshals_only(lib_path):
+    """The CPython-API module, when built, exposes the four per-step calls
+    and checks only the argument list (a wrong one fails before any call)."""
+    import paged_kv_cache_21_gb300 as pk
+    if not pk.fast_path():
+        pytest.skip("no Python headers here: the ctypes binding serves every call")
+    import paged_kv_cache_21_gb300._pkvfast as fast
+    for name, n in (("paged_decode", 26), ("paged_decode_step", 22),
+                    ("paged_decode_attention", 20), ("kv_append", 13)):
+        fn = getattr(fast, name)
+        with pytest.raises(TypeError):
+            fn(*([0] * (n - 1)))
+        with pytest.raises(TypeError):
+            fn(*([0] * (n + 1)))
+    # the module links the library the ctypes handle loaded, not a copy
+    out = subprocess.run(["ldd", fast.__file__], capture_output=True, text=True).stdout
+    assert "libpagedkv.so" in out and os.path.dirname(lib_path) in out

@@ -849,3 +849,35 @@ def test_readme_usage_example_runs():
     assert list(env["lens"]) == [1, 1]
     # one key per sequence: each query head returns its KV head's new V exactly
     assert torch.equal(env["out"], env["v_new"].repeat_interleave(4, dim=1))
+
+
+def test_fast_calls_match_ctypes_calls_and_share_the_library():
+    """The per-step calls through the CPython-API module and through ctypes
+    reach the same library instance: same output bits, and a device flag
+    raised by a fast call is what kv_get_device_error (ctypes) reports."""
+    import paged_kv_cache_21_gb300 as pk
+    if not pk.fast_path():
+        pytest.skip("fast-call module not built")
+    case = workloads.make_custom(4, 32, 8, 128, [17, 300, 4097, 1000], seed=52)
+    out_f, kc, vc = H.gpu_step(case, fused=True, early_inputs=True)
+    bt = torch.from_numpy(case.block_tables).cuda()
+    cl = torch.from_numpy(case.context_lens).cuda()
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    out_c = torch.empty_like(out_f)
+    L = pk._lib
+    s = torch.cuda.current_stream().cuda_stream
+    kn, vn, q = case.k_new.cuda(), case.v_new.cuda(), case.q.cuda()
+    rc = L.paged_decode(out_c.data_ptr(), pk.BF16, q.data_ptr(), kn.data_ptr(), vn.data_ptr(),
+                        kc.data_ptr(), vc.data_ptr(), pk.BF16, 1.0, 1.0, case.num_blocks,
+                        bt.data_ptr(), bt.shape[1], cl.data_ptr(), case.B, case.Hq, case.Hkv,
+                        case.D, case.scale, None, None, 0, pk.DECODE_EARLY_INPUTS,
+                        ws.data_ptr(), ws.numel(), s)
+    assert rc == pk.KV_OK
+    torch.cuda.synchronize()
+    assert torch.equal(out_c.view(torch.int16), out_f.view(torch.int16))
+    pk.get_device_error()
+    bad = bt.clone()
+    bad[1, 0] = case.num_blocks + 7
+    pk.paged_decode(out_c, q, kc, vc, bad, cl, case.scale, ws)
+    torch.cuda.synchronize()
+    assert pk.get_device_error() == (pk.DEVERR_BLOCK_OUT_OF_RANGE, case.num_blocks + 7)
