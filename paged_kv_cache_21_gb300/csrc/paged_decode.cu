@@ -1434,7 +1434,48 @@ int tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000& fn)
 
 // Tensor map over a cache viewed as [num_blocks*Hkv][16][D]; one box is 16
 // token rows x (128 or 64) bytes, swizzled to match tile_off().
+// A tensor map is a pure function of (base address, head dim, element type,
+// blocks, KV heads), so the last few are kept: a decode loop calls with the
+// same caches every step and skips the encode.  (Virtual addresses are
+// unique across the devices of a process.)
+struct MapEntry {
+    const void* base;
+    int D, fp8, num_blocks, Hkv;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 8;
+MapEntry g_maps[kMapCache];
+int g_map_count = 0, g_map_next = 0;
+std::mutex g_map_mu;
+
+int encode_cache_map(CUtensorMap* map, const void* base, int D, bool fp8, int num_blocks,
+                     int Hkv);
+
 int make_cache_map(CUtensorMap* map, const void* base, int D, bool fp8, int num_blocks, int Hkv)
+{
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_map_count; ++i) {
+        const MapEntry& e = g_maps[i];
+        if (e.base == base && e.D == D && e.fp8 == (int)fp8 && e.num_blocks == num_blocks &&
+            e.Hkv == Hkv) {
+            *map = e.map;
+            return KV_OK;
+        }
+    }
+    if (int rc = encode_cache_map(map, base, D, fp8, num_blocks, Hkv)) return rc;
+    MapEntry& e = g_maps[g_map_next];
+    e.base = base;
+    e.D = D;
+    e.fp8 = (int)fp8;
+    e.num_blocks = num_blocks;
+    e.Hkv = Hkv;
+    e.map = *map;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    if (g_map_count < kMapCache) ++g_map_count;
+    return KV_OK;
+}
+
+int encode_cache_map(CUtensorMap* map, const void* base, int D, bool fp8, int num_blocks, int Hkv)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     if (int rc = tensor_map_encoder(enc)) return rc;
