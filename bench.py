@@ -34,10 +34,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "a8cd396d1cfc1761285a3defd8930b4a39582ebe7f53c4713974bca0a9eaf82a",
-           "bytes_per_launch": 1087639552,
+TRAFFIC = {"kernel_sha256": "33345e5c784bf22118c7bf7d5bd09e4004317648a09aa9b5b4c96fac18439cb7",
+           "bytes_per_launch": 1088765952,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,145,344 B + 2,764,544 B), scaled x4 by units processed "
+                     "(269,145,344 B + 3,046,144 B), scaled x4 by units processed "
                      "(profiles/paged_decode_split_b8_full.md)"}
 
 
