@@ -163,9 +163,10 @@ def test_edge_lengths(D, G, kv_dtype):
     check_case(case, what="fused D%d G%d dt%d" % (D, G, kv_dtype), fused=True)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (64, 2)])
 @pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
 @pytest.mark.parametrize("max_len", [40, 300, 600, 2000])
-def test_narrow_tables_spread_over_more_warps(max_len, kv_dtype):
+def test_narrow_tables_spread_over_more_warps(max_len, kv_dtype, Hq, Hkv):
     """A block table of w columns sets the minimum range of a warp to
     clamp(ceil(w / 8), 2, 16) blocks: 2, 3, 5 and 16 here (odd and even
     ranges), so short sequences are cut across several warps and merged;
@@ -173,7 +174,7 @@ def test_narrow_tables_spread_over_more_warps(max_len, kv_dtype):
     rng = np.random.default_rng(max_len)
     lens = rng.integers(1, max_len + 1, size=24)
     lens[0] = max_len
-    case = workloads.make_custom(24, 32, 8, 128, lens, kv_dtype=kv_dtype, seed=max_len + 1)
+    case = workloads.make_custom(24, Hq, Hkv, 128, lens, kv_dtype=kv_dtype, seed=max_len + 1)
     assert case.block_tables.shape[1] == -(-max_len // 16)
     check_case(case, what="w=%d" % case.block_tables.shape[1])
     check_case(case, what="fused early w=%d" % case.block_tables.shape[1], fused=True,
