@@ -7,8 +7,15 @@ prefilled tokens + 1 appended (8193), 16-token blocks scattered at random in a
 shared pool.  KV read per step: 1,073,872,896 bytes (larger than the 129 MB
 L2, so no flush is needed between steps).
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU float64
-oracle instead, on a bounded sample of the same workload.
+Prints one JSON line (rank 0).  ``value`` is the device-timed loop of the
+library's fused call (``paged_decode`` with the append and early inputs);
+``e2e`` is the same step through ``DecodeStepStaging`` with the inputs copied
+from pinned host memory and the output copied back every step (host-ordered
+uploads; ``e2e.stream_ordered`` and ``e2e.zero_copy`` beside it);
+``graph_replay`` times CUDA-graph replays; ``roofline`` relates the split
+kernel's event-timed duration to the measured copy bandwidth.
+``--impl reference`` times the CPU float64 oracle instead, on a bounded sample
+of the same workload.
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
 scaling, no data-path collective); the step time is the max over ranks and
