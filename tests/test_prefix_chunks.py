@@ -128,3 +128,40 @@ def test_min_blocks_and_bad_arguments(pk):
         pk.prefix_chunks(case.block_tables, case.context_lens, 4, min_blocks=0)
     empty_c, empty_s = pk.prefix_chunks(np.zeros((0, 4), np.int32), np.zeros(0, np.int32), 4)
     assert empty_c.shape[0] == 0 and empty_s.shape[0] == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_prefix_trees_obey_every_rule(pk, seed):
+    """Random block tables: groups share random runs of leading blocks
+    (prefixes of one another, a tree), some sequences stand alone, some are
+    empty; every table kv_prefix_chunks builds obeys the rules, and a chunk
+    never spans two groups."""
+    rng = np.random.default_rng(1000 + seed)
+    G = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.integers(2, 60))
+    mb = 40
+    bt = np.full((B, mb), -1, dtype=np.int32)
+    lens = np.zeros(B, dtype=np.int32)
+    next_id = 0
+    group_of = rng.integers(0, max(1, B // 4), size=B)
+    trunks = {}
+    for s in range(B):
+        g = int(group_of[s])
+        if g not in trunks:
+            trunks[g] = list(range(next_id, next_id + mb))
+            next_id += mb
+        if rng.random() < 0.15:
+            continue                                    # empty context
+        L = int(rng.integers(1, 16 * mb + 1))
+        nb = -(-L // 16)
+        run = int(rng.integers(0, nb + 1))              # leading blocks taken from the trunk
+        row = trunks[g][:run] + list(range(next_id, next_id + nb - run))
+        next_id += nb - run
+        bt[s, :nb] = row
+        lens[s] = L
+    min_blocks = int(rng.integers(1, 4))
+    chunks, seq_chunk = pk.prefix_chunks(bt, lens, G, min_blocks=min_blocks)
+    check_table(bt, lens, G, chunks, seq_chunk, min_blocks=min_blocks)
+    for row in chunks:
+        members = [int(x) for x in row[2:2 + int(row[1])]]
+        assert len({int(group_of[s]) for s in members}) == 1
