@@ -105,7 +105,11 @@ def build_fast(force=False):
            PYEXT_SRC, "-o", tmp, "-L", PKG, "-l:libpagedkv.so", "-Wl,-rpath,$ORIGIN"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError("compile failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
+        # optional: the ctypes binding serves every call without it
+        import sys
+        print("warning: _pkvfast not built (%s):\n%s" % (" ".join(cmd), r.stderr),
+              file=sys.stderr)
+        return None
     os.replace(tmp, out)
     return out
 
