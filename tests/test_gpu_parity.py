@@ -219,8 +219,8 @@ def test_mqa_full_size_and_deterministic(Hq):
     two runs bit-identical."""
     import paged_kv_cache_21_gb300 as pk
     case = workloads.make_custom(32, Hq, 1, 128, [8193] * 32, seed=Hq)
-    out1 = check_case(case, what="MQA %d" % Hq, fused=True, early_inputs=True)
-    assert out1 < 2e-3
+    check_case(case, what="MQA %d" % Hq, fused=True, early_inputs=True)
+    check_case(case, what="MQA %d f32" % Hq, out_dtype=torch.float32)
     o1, _, _ = H.gpu_step(case, fused=True, early_inputs=True)
     o2, _, _ = H.gpu_step(case, fused=True, early_inputs=True)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
