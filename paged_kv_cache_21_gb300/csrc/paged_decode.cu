@@ -139,6 +139,8 @@ struct DecodeParams {
     const uint16_t* v_new;
     uint8_t* k_cache;        // caches, written only by the fused append
     uint8_t* v_cache;
+    // Hkv and G count virtual KV heads and their rows (groups above 16 rows
+    // are cut into sub-groups, see hshift)
     int B, Hq, Hkv, G, max_blocks, num_blocks;
     int warps_total;
     int min_q1;              // minimum range of a warp in the sequence phase
