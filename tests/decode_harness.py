@@ -149,15 +149,3 @@ def compare(case, out_gpu, ref, pair_select=None, what=""):
     assert not bad.any(), "%s: %d elements beyond tolerance, max err %.3g (tol %.3g)" % (
         what, int(bad.sum()), float(err.max()), tol)
     return float(err.max())
-
-
-def sample_pairs(case, n, seed=0):
-    """A seeded sample of (sequence, KV head) pairs, always including the
-    first and the last pair and the longest sequence."""
-    rng = np.random.default_rng(seed)
-    sel = np.zeros((case.B, case.Hkv), dtype=bool)
-    flat = rng.choice(case.B * case.Hkv, size=min(n, case.B * case.Hkv), replace=False)
-    sel.reshape(-1)[flat] = True
-    sel[0, 0] = sel[-1, -1] = True
-    sel[int(np.argmax(case.context_lens)), 0] = True
-    return sel
