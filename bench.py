@@ -64,6 +64,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (profiling a smaller case)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block (the other workloads, one after another)")
+    ap.add_argument("--ref-seqs", type=int, default=4,
+                    help="sequences of the workload per reference-arm step")
     ap.add_argument("--prefix", action="store_true",
                     help="also time the shared-prefix step (paged_decode with the chunks "
                          "kv_prefix_chunks finds) beside the plain one")
@@ -260,7 +264,8 @@ def run_reference(args):
         return 0
     import oracle
     import workloads
-    case = oracle_sample_case(args.config, 1)
+    spec = workloads.CONFIGS[args.config]
+    case = oracle_sample_case(args.config, max(2, args.ref_seqs))
     prep = oracle_prepare(case)
     for _ in range(max(args.warmup, 0)):
         oracle_step(case, prep)
@@ -270,24 +275,30 @@ def run_reference(args):
     el = time.perf_counter() - t0
     ms = el / args.steps * 1e3
     gbs = case.logical_kv_bytes() / (ms * 1e-3) / 1e9
-    spec = workloads.CONFIGS[args.config]
-    sample = ("1 of %d sequences of the workload per step (%d KV heads x %d tokens, %d bytes of "
-              "KV), float64 C oracle with OpenMP" % (spec["B"], case.Hkv,
-                                                     int(case.context_lens[0]),
-                                                     case.logical_kv_bytes()))
+    sample = ("%d of %d sequences of the workload per step (%d (sequence, KV head) pairs, %d "
+              "bytes of KV), float64 C oracle with OpenMP over the pairs"
+              % (case.B, spec["B"], case.B * case.Hkv, case.logical_kv_bytes()))
     # n_gpus is the launch's N, as in our arm's line; the oracle itself uses
     # the host cores of rank 0 and no GPU
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
             "n_gpus": max(world, args.gpus), "gpu_used": False,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(args.config, args.batch),
+            "data": "synthetic", "config": line_config(args.config, args.batch,
+                                                       max(world, args.gpus)),
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "kind": "oracle",
                              "cores": oracle.max_threads(), "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def line_config(cfg, batch, world):
+    """The `config` of the JSON line: the workload plus how it is run (the
+    same dict for both arms)."""
+    return dict(workload_config(cfg, batch),
+                parallelism="replicas x%d" % world if world > 1 else "single GPU")
 
 
 def workload_config(cfg, batch=None):
@@ -312,6 +323,135 @@ def workload_config(cfg, batch=None):
 
 # -------------------------------------------------------------- our arm
 
+def timed_loop(K, body, nev, stream, world, tail=None):
+    """Run exactly K steps between a barrier + sync on both sides; events
+    ev[i][0..nev-1] (created and recorded once beforehand, so their handles
+    exist) are handed to the body of step i; `tail` runs before the end event
+    is recorded (to join work on other streams).  Returns (ms per step, ev)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    t_beg = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_beg.record(stream)
+    for i in range(K):
+        body(ev[i])
+    if tail is not None:
+        tail()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return t_beg.elapsed_time(t_end) / K, ev
+
+
+def device_case(pk, case, device):
+    """Device tensors of one decode step of `case`: caches filled through
+    kv_append with the pool, tables, lengths, q, new K/V, output, workspace."""
+    import torch
+    import workloads
+    cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
+    kc = torch.empty((case.num_blocks, case.Hkv, 16, case.D), dtype=cdt, device=device)
+    vc = torch.empty_like(kc)
+    pk.kv_append(case.pool_k.to(device), case.pool_v.to(device), kc, vc,
+                 torch.arange(case.num_blocks * 16, dtype=torch.int64, device=device),
+                 case.k_scale, case.v_scale)
+    case.pool_k = case.pool_v = None
+    torch.cuda.synchronize()
+    return dict(kc=kc, vc=vc, bt=torch.from_numpy(case.block_tables).to(device),
+                cl=torch.from_numpy(case.context_lens).to(device), q=case.q.to(device),
+                k_new=case.k_new.to(device), v_new=case.v_new.to(device),
+                out=torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=device),
+                ws=pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D, case.kv_dtype,
+                                      device=device))
+
+
+def measure_fused(pk, case, t, stream, K, W, world):
+    """The benchmark's step (paged_decode: fused append, early inputs) timed
+    as K back-to-back steps, then the same loop through paged_decode_timed
+    with events before the split kernel, after it and after the merge, for
+    the split kernel's own duration in the same mode."""
+    def step():
+        pk.paged_decode(t["out"], t["q"], t["kc"], t["vc"], t["bt"], t["cl"], case.scale, t["ws"],
+                        case.k_scale, case.v_scale, k_new=t["k_new"], v_new=t["v_new"],
+                        early_inputs=True, stream=stream)
+
+    def step_ev(e):
+        pk.paged_decode_timed(t["out"], t["q"], t["kc"], t["vc"], t["bt"], t["cl"], case.scale,
+                              t["ws"], e, case.k_scale, case.v_scale, k_new=t["k_new"],
+                              v_new=t["v_new"], early_inputs=True, stream=stream)
+
+    for _ in range(W):
+        step()
+    ms_local, _ = timed_loop(K, lambda e: step(), 0, stream, world)
+    for _ in range(W):
+        step_ev([None, None, None])
+    ev_ms, ev = timed_loop(K, step_ev, 3, stream, world)
+    split_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    merge_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    return {"ms_local": ms_local, "split_ms": split_ms, "merge_ms": merge_ms,
+            "evented_ms_per_step": ev_ms}
+
+
+def read_ceiling(pk, device, stream, nbytes=1 << 30, reps=10):
+    """Same-run read-only ceiling: kv_read_ceiling streams a 1 GiB buffer
+    through shared memory in the decode kernel's bulk-copy pattern."""
+    import torch
+    buf = torch.ones(nbytes // 2, dtype=torch.int16, device=device)
+    sink = torch.zeros(2, dtype=torch.int32, device=device)
+    for _ in range(3):
+        pk.read_ceiling(buf, sink, stream=stream)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(reps):
+        pk.read_ceiling(buf, sink, stream=stream)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    assert int(sink[1]) == 0, "read ceiling: a bulk copy timed out"
+    gbs = reps * nbytes / (r0.elapsed_time(r1) * 1e-3) / 1e9
+    del buf, sink
+    return {"gbs": gbs, "how": "kv_read_ceiling: 1 GiB streamed into shared memory by bulk "
+                               "copies in the decode kernel's pattern (persistent grid, 4 warps "
+                               "x 3 x 8 KB stages per CTA, evict-first), no arithmetic; bytes "
+                               "read only; mean of %d launches" % reps}
+
+
+def per_config(pk, cfgs, device, stream, K, W, world, peak, read_gbs):
+    """Each of the other workloads on its own: fused step time, split and
+    merge durations in the same loop mode, KV GB/s and the fractions of the
+    measured copy peak and of the same-run read ceiling."""
+    import torch
+    import workloads
+    res = {}
+    for cfg in cfgs:
+        case = workloads.make_case(cfg, device=device)
+        t = device_case(pk, case, device)
+        m = measure_fused(pk, case, t, stream, K, W, world)
+        flags, detail = pk.get_device_error()
+        assert flags == 0, "config %s: device error flags %d (detail %d)" % (cfg, flags, detail)
+        ms = reduce_max(m["ms_local"], world, device)
+        kvb = case.logical_kv_bytes()
+        gbs = kvb / (ms * 1e-3) / 1e9
+        split_gbs = kvb / (m["split_ms"] * 1e-3) / 1e9
+        r = {"config": workload_config(cfg), "us_per_step": ms * 1e3,
+             "kv_bytes_per_step": kvb, "kv_gbs": gbs,
+             "frac_of_copy_peak": gbs / peak, "frac_of_read_ceiling": gbs / read_gbs,
+             "split_us": m["split_ms"] * 1e3, "merge_us": m["merge_ms"] * 1e3,
+             "split_gbs": split_gbs, "split_frac_of_copy_peak": split_gbs / peak}
+        if cfg == "3":
+            r["kv_bytes_unique"] = case.unique_kv_bytes()
+        if kvb < 129e6:
+            r["note"] = "L2-resident latency case: GB/s is nominal"
+        res[cfg] = r
+        del t
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -329,25 +469,14 @@ def run_ours(args):
     case = workloads.make_case(cfg, device=device,
                                override={"B": args.batch} if args.batch else None)
     B, Hq, Hkv, D = case.B, case.Hq, case.Hkv, case.D
-    NB = case.num_blocks
-    cdt = torch.bfloat16 if case.kv_dtype == workloads.BF16 else torch.uint8
-    kc = torch.empty((NB, Hkv, 16, D), dtype=cdt, device=device)
-    vc = torch.empty_like(kc)
-    pk.kv_append(case.pool_k, case.pool_v, kc, vc,
-                 torch.arange(NB * 16, dtype=torch.int64, device=device),
-                 case.k_scale, case.v_scale)
-    case.pool_k = case.pool_v = None
-    torch.cuda.synchronize()
-
+    t = device_case(pk, case, device)
+    kc, vc, bt, cl = t["kc"], t["vc"], t["bt"], t["cl"]
+    q, k_new, v_new, out, ws = t["q"], t["k_new"], t["v_new"], t["out"], t["ws"]
     slots_np = pk.slot_mapping(case.block_tables, case.context_lens.astype(np.int64) - 1)
     slots = torch.from_numpy(slots_np).to(device)
-    bt = torch.from_numpy(case.block_tables).to(device)
-    cl = torch.from_numpy(case.context_lens).to(device)
-    q, k_new, v_new = case.q, case.k_new, case.v_new
-    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
-    ws = pk.alloc_workspace(B, Hq, Hkv, D, case.kv_dtype, device=device)
     stream = torch.cuda.current_stream(device)
     kv_bytes = case.logical_kv_bytes()
+    W = max(args.warmup, 3)
 
     def step():
         # one decode step of the layer in a decode loop: append the new token
@@ -368,39 +497,15 @@ def run_ours(args):
         pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
                                         case.k_scale, case.v_scale, stream=stream)
 
-    def step_split_timed(evs):
-        pk.paged_decode_attention_timed(out, q, kc, vc, bt, cl, case.scale, ws, evs,
-                                        case.k_scale, case.v_scale, stream=stream)
-
     def timed(K, body, nev, tail=None):
-        """Run exactly K steps between a barrier + sync on both sides; events
-        ev[i][0..nev-1] are handed to the body of step i; `tail` runs before
-        the end event is recorded (to join work on other streams)."""
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
-        for e in ev:                  # create the event handles before the timed region
-            for x in e:
-                x.record(stream)
-        t_beg = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        t_beg.record(stream)
-        for i in range(K):
-            body(ev[i])
-        if tail is not None:
-            tail()
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        return t_beg.elapsed_time(t_end) / K, ev
+        return timed_loop(K, body, nev, stream, world, tail=tail)
 
     def unfused_body(e):
         e[0].record(stream)
         step_unfused(e[1:])
 
     # warm-up (W >= 3), then a short untimed soak while the clock sampler runs
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(W):
         step()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
@@ -421,50 +526,54 @@ def run_ours(args):
     flags, detail = pk.get_device_error()
     assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
 
+    # the split kernel's own duration in the same loop (fused append, early
+    # inputs), from events recorded before and after it in every step
+    fm = measure_fused(pk, case, t, stream, K, W, world)
+    split_ms, merge_ms = fm["split_ms"], fm["merge_ms"]
+
     # the same loop with the default ordering (every read after the previous
     # kernel completes: paged_decode_step)
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(W):
         step_default()
     dms_local, _ = timed(K, lambda e: step_default(), 0)
     default_step_us = reduce_max(dms_local, world, device) * 1e3
-
-    # per-kernel durations: the same kernels with events around each launch
-    for _ in range(max(args.warmup, 3)):
-        step_split_timed([None, None, None])
-    _, sp_ev = timed(K, step_split_timed, 3)
-    split_ms = statistics.mean(sp_ev[i][0].elapsed_time(sp_ev[i][1]) for i in range(K))
-    merge_ms = statistics.mean(sp_ev[i][1].elapsed_time(sp_ev[i][2]) for i in range(K))
 
     # shared-prefix step: the chunk table is built once on the host from the
     # block tables (kv_prefix_chunks), the step reads each shared tile once
     # per chunk of sequences
     prefix = None
     if args.prefix:
-        chunks_np, seq_chunk_np = pk.prefix_chunks(case.block_tables, case.context_lens,
-                                                   Hq // Hkv)
-        nc = len(chunks_np)
-        dch = torch.from_numpy(chunks_np).to(device)
-        dsc = torch.from_numpy(seq_chunk_np).to(device)
-        wsp = pk.alloc_prefix_workspace(B, nc, Hq, Hkv, D, case.kv_dtype, device=device)
+        def time_chunks(chunks_np, seq_chunk_np):
+            nc = len(chunks_np)
+            dch = torch.from_numpy(chunks_np).to(device) if nc else None
+            dsc = torch.from_numpy(seq_chunk_np).to(device) if nc else None
+            wsp = pk.alloc_prefix_workspace(B, nc, Hq, Hkv, D, case.kv_dtype, device=device)
 
-        def step_prefix():
-            pk.paged_decode(out, q, kc, vc, bt, cl, case.scale, wsp, case.k_scale,
-                            case.v_scale, k_new=k_new, v_new=v_new, chunks=dch, seq_chunk=dsc,
-                            early_inputs=True, stream=stream)
+            def step_prefix():
+                pk.paged_decode(out, q, kc, vc, bt, cl, case.scale, wsp, case.k_scale,
+                                case.v_scale, k_new=k_new, v_new=v_new, chunks=dch,
+                                seq_chunk=dsc, early_inputs=True, stream=stream)
 
-        for _ in range(max(args.warmup, 3)):
-            step_prefix()
-        pms_local, _ = timed(K, lambda e: step_prefix(), 0)
-        pms = reduce_max(pms_local, world, device)
-        flags, detail = pk.get_device_error()
-        assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
-        read_bytes = kv_bytes - sum(int(r[0]) * (int(r[1]) - 1) for r in chunks_np) * \
-            Hkv * 2 * 16 * D * case.elem_bytes
-        prefix = {"us_per_step": pms * 1e3, "chunks": nc,
-                  "kv_gbs_logical": kv_bytes / (pms * 1e-3) / 1e9,
-                  "kv_bytes_read": read_bytes,
-                  "kv_gbs_read": read_bytes / (pms * 1e-3) / 1e9,
-                  "plain_us_per_step": ms * 1e3, "speedup_vs_plain": ms / pms}
+            for _ in range(W):
+                step_prefix()
+            pms = reduce_max(timed(K, lambda e: step_prefix(), 0)[0], world, device)
+            flags, detail = pk.get_device_error()
+            assert flags == 0, "device error flags %d (detail %d)" % (flags, detail)
+            read_bytes = kv_bytes - sum(int(r[0]) * (int(r[1]) - 1) for r in chunks_np) * \
+                Hkv * 2 * 16 * D * case.elem_bytes
+            return {"us_per_step": pms * 1e3, "chunks": nc,
+                    "kv_gbs_logical": kv_bytes / (pms * 1e-3) / 1e9,
+                    "kv_bytes_read": read_bytes,
+                    "kv_gbs_read": read_bytes / (pms * 1e-3) / 1e9,
+                    "plain_us_per_step": ms * 1e3, "speedup_vs_plain": ms / pms}
+
+        # the library's decision (kv_prefix_plan: chunks only where they pay),
+        # and every chunk kv_prefix_chunks finds, used regardless
+        prefix = time_chunks(*pk.prefix_plan(case.block_tables, case.context_lens, Hq, Hkv, D,
+                                             case.kv_dtype))
+        prefix["how"] = "kv_prefix_plan"
+        prefix["all_chunks"] = time_chunks(*pk.prefix_chunks(case.block_tables,
+                                                             case.context_lens, Hq // Hkv))
 
     # one fused step captured in a CUDA graph and replayed, each replay
     # bracketed by events: the median is the per-layer-step latency
@@ -483,7 +592,7 @@ def run_ours(args):
     g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(n_rep)]
     with torch.cuda.stream(gs):
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(W):
             graph.replay()
         for a, b in g_ev:
             a.record(gs)
@@ -525,7 +634,7 @@ def run_ours(args):
     del graph
 
     # the same step as separate launches (kv_append, then paged_decode_attention)
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(W):
         step_unfused([None, None, None])
     un_ms_local, un_ev = timed(K, unfused_body, 4)
     unfused = {"us_per_step": reduce_max(un_ms_local, world, device) * 1e3,
@@ -562,7 +671,7 @@ def run_ours(args):
                          stream=stream)
                 counter[0] += 1
 
-            for _ in range(max(args.warmup, 3)):
+            for _ in range(W):
                 e2e_step()
             torch.cuda.synchronize()
             # the end event waits for the last download on its copy stream
@@ -601,7 +710,7 @@ def run_ours(args):
             zc.step(zcount[0], kc, vc, case.scale, case.k_scale, case.v_scale, stream=stream)
             zcount[0] += 1
 
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(W):
             zc_step()
         torch.cuda.synchronize()
         zc_ms = reduce_max(timed(K, zc_step, 0)[0], world, device)
@@ -631,6 +740,8 @@ def run_ours(args):
                     "how": "torch copy_ of a 1 GiB buffer, read + write bytes, same run"}
     del src, dst
 
+    rc = read_ceiling(pk, device, stream)
+
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     # the recorded counters belong to the default workload (config 2, batch 32)
@@ -645,22 +756,31 @@ def run_ours(args):
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
                 "split_us": split_ms * 1e3, "merge_us": merge_ms * 1e3,
-                "copy_ceiling": copy_ceiling}
+                "split_timing": "events before and after the split kernel in every step of "
+                                "the benchmark's loop (paged_decode_timed: fused append, "
+                                "early inputs); %.1f us per step with the events"
+                                % (fm["evented_ms_per_step"] * 1e3),
+                "copy_ceiling": copy_ceiling, "read_ceiling": rc,
+                "frac_vs_read_ceiling": achieved / rc["gbs"],
+                "step_frac_vs_read_ceiling": (kv_bytes / (ms * 1e-3) / 1e9) / rc["gbs"]}
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-            "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "warmup": W, "ms_per_step": ms,
             "us_per_layer_step": ms * 1e3, "pct_of_hbm_peak": 100.0 * (kv_bytes / (ms * 1e-3)
                                                                       / 1e9) / peak,
             "pct_of_8tbs_nameplate": 100.0 * (kv_bytes / (ms * 1e-3) / 1e9) / 8000.0,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if case.kv_dtype == workloads.BF16 else "e4m3",
             "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
-            "config": dict(workload_config(cfg, args.batch),
-                           parallelism="replicas x%d" % world if world > 1 else "single GPU"),
+            "config": line_config(cfg, args.batch, world),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
             "decode_call": "paged_decode (fused append, KV_DECODE_EARLY_INPUTS)",
             "default_step_us": default_step_us,
             "unfused": unfused, "graph_replay": graph_replay}
+    if not args.no_per_config and not args.batch:
+        others = [c for c in ("1", "2", "3", "4", "5a", "5b") if c != cfg]
+        line["per_config"] = per_config(pk, others, device, stream, K, W, world, peak,
+                                        rc["gbs"])
     if prefix is not None:
         line["prefix"] = prefix
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -418,6 +418,25 @@ int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* context_lens, int num_seqs, int group_size, int min_blocks,
                      int32_t* chunks, int32_t* seq_chunk, int* num_chunks);
 
+/* kv_prefix_chunks with the decision whether the chunks pay (host memory):
+ * returns the chunk table kv_prefix_chunks builds (group_size = num_q_heads /
+ * num_kv_heads, min_blocks 1) when its chunks save at least 6 % of the
+ * blocks the step reads and the step has more (sequence, KV head) pairs than
+ * the split-KV kernel has resident warps; otherwise *num_chunks = 0 and
+ * seq_chunk all -1, i.e. plain decoding.  (Measured crossovers of this
+ * implementation: below either bound the shared-prefix kernel, which carries
+ * two row tiles of state, is slower than reading the shared blocks once per
+ * sequence -- which, with few pairs, mostly hit L2 anyway.)  resident_warps:
+ * the split kernel's warps, or <= 0 to query the current device (152 SMs x 2
+ * CTAs x 4 warps = 1216 on GB300 at d128).  Groups of more than 8 query
+ * heads per KV head always get plain decoding.  chunks: num_seqs / 2 rows;
+ * seq_chunk: num_seqs entries.  Returns KV_OK, KV_ERR_INVALID_ARG,
+ * KV_ERR_UNSUPPORTED (shape) or KV_ERR_CUDA (device query). */
+int kv_prefix_plan(const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                   int head_dim, int kv_dtype, int resident_warps, int32_t* chunks,
+                   int32_t* seq_chunk, int* num_chunks);
+
 /* Workspace bytes paged_decode needs with num_chunks prefix chunks (as
  * paged_decode_workspace_bytes, which is the num_chunks == 0 case). */
 int paged_decode_prefix_workspace_bytes(int num_seqs, int num_chunks, int num_q_heads,
@@ -462,7 +481,45 @@ int paged_decode(void* out, int out_dtype, const void* q, const void* k_new, con
                  int num_chunks, unsigned flags, void* workspace, size_t workspace_bytes,
                  void* stream);
 
+/* The same step as paged_decode, with events recorded on the stream before
+ * the split-KV kernel, after it, and after the merge kernel (each may be
+ * NULL), so that a caller can time the split kernel inside a loop of
+ * consecutive decode steps in the mode it normally runs in (fused append,
+ * KV_DECODE_EARLY_INPUTS).  A measurement hook of this implementation (the
+ * pages have no counterpart); an event record between the two kernels may
+ * delay the merge kernel's start by a launch latency. */
+int paged_decode_timed(void* out, int out_dtype, const void* q, const void* k_new,
+                       const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                       float k_scale, float v_scale, int num_blocks,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, float scale, const int32_t* chunks,
+                       const int32_t* seq_chunk, int num_chunks, unsigned flags,
+                       void* workspace, size_t workspace_bytes, void* stream, void* ev_begin,
+                       void* ev_split_end, void* ev_end);
+
+/* Read-only bandwidth ceiling (a measurement hook; the pages have no
+ * counterpart): streams `bytes` of device memory at `buf` into shared memory
+ * with bulk copies and no arithmetic, in the decode kernel's own pattern (a
+ * persistent grid, per-warp rings of 3 x 8 KB stages, equal contiguous ranges
+ * per warp, L2 evict-first), so its bandwidth bounds what the decode kernel
+ * can reach.  buf: device, 16-byte aligned; bytes: a positive multiple of 16;
+ * sink: device, 2 words the caller zeroes -- sink[0] receives an XOR of the
+ * data read, sink[1] becomes 1 if a copy never arrived (bounded wait).
+ * Asynchronous on `stream`.  Returns KV_OK, KV_ERR_INVALID_ARG or KV_ERR_CUDA. */
+int kv_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream);
+
 /* ------------------------------------------------------------- diagnostics */
+
+/* Test hook (no counterpart in the pages): while `cycles` > 0, every warp of
+ * the split-KV kernels launched afterwards makes the first wait of its range
+ * on a barrier that nothing arrives on, gives up after `cycles` SM clocks
+ * and takes the time-out path -- KV_DEVERR_PIPELINE_TIMEOUT raised, the bulk
+ * copies it has issued waited for at the normal limit, the warp stops, so
+ * that call's output is undefined.  It lets a test see the flag without a
+ * copy that really never arrives.  0 (the default) turns it off; a value
+ * outside [0, 2^31] returns KV_ERR_INVALID_ARG.  Process-wide. */
+int kv_test_pipeline_stall(long long cycles);
 
 /* Read (synchronously, on the current device) and clear the sticky device
  * error flags (KV_DEVERR_* bits) set by the kernels' bounds checks; *detail

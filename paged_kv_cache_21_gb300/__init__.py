@@ -97,10 +97,16 @@ _SIGS = {
     "paged_decode_attention_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i,
                                             _i, _i, _i, _f, _p]),
     "kv_prefix_chunks": (_i, [_p, _i, _p, _i, _i, _i, _p, _p, ctypes.POINTER(_i)]),
+    "kv_prefix_plan": (_i, [_p, _i, _p, _i, _i, _i, _i, _i, _i, _p, _p, ctypes.POINTER(_i)]),
     "paged_decode_prefix_workspace_bytes": (_i, [_i, _i, _i, _i, _i, _i,
                                                  ctypes.POINTER(ctypes.c_size_t)]),
     "paged_decode": (_i, [_p, _i, _p, _p, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i, _i,
                           _i, _f, _p, _p, _i, ctypes.c_uint, _p, ctypes.c_size_t, _p]),
+    "paged_decode_timed": (_i, [_p, _i, _p, _p, _p, _p, _p, _i, _f, _f, _i, _p, _i, _p, _i, _i,
+                                _i, _i, _f, _p, _p, _i, ctypes.c_uint, _p, ctypes.c_size_t, _p,
+                                _p, _p, _p]),
+    "kv_read_ceiling": (_i, [_p, ctypes.c_size_t, _p, _p]),
+    "kv_test_pipeline_stall": (_i, [ctypes.c_longlong]),
     "kv_get_device_error": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_i64)]),
     "kv_version": (ctypes.c_char_p, []),
 }
@@ -428,6 +434,26 @@ def prefix_chunks(block_tables, context_lens, group_size, min_blocks=1):
     return chunks[:nc.value].copy(), seq_chunk[:B].copy()
 
 
+def prefix_plan(block_tables, context_lens, num_q_heads, num_kv_heads, head_dim,
+                kv_dtype=BF16, resident_warps=0):
+    """prefix_chunks with the library's decision whether shared-prefix
+    decoding pays for these tables (kv_prefix_plan; resident_warps 0: those
+    of the current device): (chunks int32 [nc, 18], seq_chunk int32 [B]),
+    nc == 0 for plain decoding."""
+    import numpy as np
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, mb = bt.shape
+    chunks = np.full((max(B // 2, 1), PREFIX_CHUNK_INTS), -1, dtype=np.int32)
+    seq_chunk = np.full(max(B, 1), -1, dtype=np.int32)
+    nc = ctypes.c_int(0)
+    _check(_lib.kv_prefix_plan(_np_ptr(bt), mb, _np_ptr(cl), B, int(num_q_heads),
+                               int(num_kv_heads), int(head_dim), int(kv_dtype),
+                               int(resident_warps), _np_ptr(chunks),
+                               _np_ptr(seq_chunk), ctypes.byref(nc)), "kv_prefix_plan")
+    return chunks[:nc.value].copy(), seq_chunk[:B].copy()
+
+
 def prefix_workspace_bytes(num_seqs, num_chunks, num_q_heads, num_kv_heads, head_dim,
                            kv_dtype=BF16):
     n = ctypes.c_size_t(0)
@@ -473,6 +499,46 @@ def paged_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, wo
         chunks.data_ptr() if nc else 0, seq_chunk.data_ptr() if nc else 0, nc,
         DECODE_EARLY_INPUTS if early_inputs else 0, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_int(stream)), "paged_decode")
+
+
+def paged_decode_timed(out, q, k_cache, v_cache, block_tables, context_lens, scale, workspace,
+                       events, k_scale=1.0, v_scale=1.0, k_new=None, v_new=None, chunks=None,
+                       seq_chunk=None, early_inputs=False, stream=None):
+    """paged_decode that also records three torch.cuda.Event objects (already
+    recorded once so that their handles exist, or None) before the split
+    kernel, after it and after the merge kernel: events = (begin, split_end,
+    end).  A measurement hook."""
+    import torch
+    B, Hq, D = q.shape
+    NB, Hkv, _, _ = k_cache.shape
+    out_dtype = F32 if out.dtype == torch.float32 else BF16
+    nc = int(chunks.shape[0]) if chunks is not None else 0
+    ev = [ctypes.c_void_p(e._as_parameter_.value) if e is not None else None for e in events]
+    _check(_lib.paged_decode_timed(
+        _dptr(out), out_dtype, _dptr(q), _dptr(k_new) if k_new is not None else None,
+        _dptr(v_new) if v_new is not None else None, _dptr(k_cache), _dptr(v_cache),
+        _cache_dtype(k_cache), float(k_scale), float(v_scale), NB, _dptr(block_tables),
+        block_tables.shape[1], _dptr(context_lens), B, Hq, Hkv, D, float(scale),
+        _dptr(chunks) if nc else None, _dptr(seq_chunk) if nc else None, nc,
+        DECODE_EARLY_INPUTS if early_inputs else 0, _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream), ev[0], ev[1], ev[2]),
+        "paged_decode_timed")
+
+
+def read_ceiling(buf, sink, stream=None):
+    """Stream the device tensor ``buf`` through shared memory with the decode
+    kernel's bulk-copy pattern and no arithmetic (kv_read_ceiling), on
+    ``stream``; ``sink`` is a zeroed int32 device tensor of 2 elements.  A
+    measurement hook: bytes / elapsed time is a read-only bandwidth ceiling."""
+    _check(_lib.kv_read_ceiling(_dptr(buf), buf.numel() * buf.element_size(), _dptr(sink),
+                                _stream_ptr(stream)), "kv_read_ceiling")
+
+
+def set_pipeline_stall(cycles):
+    """Test hook (kv_test_pipeline_stall): with cycles > 0 every split-kernel
+    warp takes the bounded-wait time-out path on its first wait; 0 turns it
+    off."""
+    _check(_lib.kv_test_pipeline_stall(int(cycles)), "kv_test_pipeline_stall")
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,

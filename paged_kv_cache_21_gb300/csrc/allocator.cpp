@@ -18,6 +18,7 @@
 #include <unordered_set>
 #include <vector>
 
+#include "internal.h"
 #include "paged_kv.h"
 
 namespace {
@@ -410,3 +411,55 @@ int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
 const char* kv_version(void) { return "pagedkv 0.1 sm_103a"; }
 
 }  // extern "C"
+
+namespace pkv {
+
+// Shared-prefix decoding trades a costlier kernel (two row tiles of state)
+// for fewer bytes.  Measured on GB300 (fused step, 32 query / 8 KV heads,
+// d128): it pays once the chunks save about 6 % of the blocks read or more,
+// and only when there are more (sequence, KV head) pairs than resident warps
+// -- with fewer, every pair starts at a warp's range start, the members of a
+// group read their shared blocks at about the same moment and the plain
+// kernel already finds them in L2.
+constexpr double kPrefixMinSavedFraction = 0.06;
+
+int prefix_plan_host(const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int group_size,
+                     int num_kv_heads, int resident_warps, int32_t* chunks, int32_t* seq_chunk,
+                     int* num_chunks)
+{
+    if (!num_chunks || num_seqs < 0 || num_kv_heads < 1 || resident_warps < 1 ||
+        group_size < 1)
+        return KV_ERR_INVALID_ARG;
+    *num_chunks = 0;
+    if (num_seqs == 0) return KV_OK;
+    if (!block_tables || !context_lens || !chunks || !seq_chunk || max_blocks_per_seq <= 0)
+        return KV_ERR_INVALID_ARG;
+    if (2 * group_size > KV_PREFIX_MAX_ROWS) {      // no chunks for groups above 8 rows
+        for (int s = 0; s < num_seqs; ++s) seq_chunk[s] = -1;
+        return KV_OK;
+    }
+    int nc = 0;
+    if (int rc = kv_prefix_chunks(block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                  group_size, 1, chunks, seq_chunk, &nc))
+        return rc;
+    if (nc == 0) return KV_OK;
+    long long saved = 0, total = 0;
+    for (int c = 0; c < nc; ++c) {
+        const int32_t* row = chunks + (int64_t)c * KV_PREFIX_CHUNK_INTS;
+        saved += (long long)row[0] * (row[1] - 1);
+    }
+    for (int s = 0; s < num_seqs; ++s) {
+        const int L = std::min(std::max(context_lens[s], 0), max_blocks_per_seq * KV_BLOCK_SIZE);
+        total += (L + KV_BLOCK_SIZE - 1) / KV_BLOCK_SIZE;
+    }
+    const long long pairs = (long long)num_seqs * num_kv_heads;
+    if ((double)saved >= kPrefixMinSavedFraction * (double)total && pairs > resident_warps) {
+        *num_chunks = nc;
+        return KV_OK;
+    }
+    for (int s = 0; s < num_seqs; ++s) seq_chunk[s] = -1;
+    return KV_OK;
+}
+
+}  // namespace pkv

@@ -61,6 +61,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -108,10 +109,13 @@ struct Geom {
     // shared memory: [stages of every warp][mbarriers][stage metadata (int4)],
     // the stage area aligned to 1024 bytes for the swizzled bulk copies
     static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
-    static constexpr int META_OFF = (BAR_OFF + kWarps * STAGES * 8 + 15) / 16 * 16;
+    // one more barrier per warp that nothing arrives on (the time-out test hook)
+    static constexpr int STALL_OFF = BAR_OFF + kWarps * STAGES * 8;
+    static constexpr int META_OFF = (STALL_OFF + kWarps * 8 + 15) / 16 * 16;
     static constexpr int SMEM = META_OFF + kWarps * STAGES * 16 + 1024;
     static_assert(TILE % 1024 == 0 && BOXB % 512 == 0, "swizzled tiles need aligned stages");
-    static_assert(BAR_OFF % 8 == 0 && META_OFF % 16 == 0, "barrier / metadata alignment");
+    static_assert(BAR_OFF % 8 == 0 && STALL_OFF % 8 == 0 && META_OFF % 16 == 0,
+                  "barrier / metadata alignment");
     static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -157,6 +161,7 @@ struct DecodeParams {
     int prow;                    // rows per partial slot
     int slot_base;               // first partial slot of the sequence phase
     int early;                   // read the host-made inputs and caches before the wait
+    long long test_stall;        // > 0: test hook, see kv_test_pipeline_stall
 };
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane)
@@ -363,8 +368,8 @@ __device__ __forceinline__ int out_dim(int i, int g, int half)
 // 2t+1, 2t+8, 2t+9) and rescales the accumulators.
 template <int D, int NBK, int NR>
 __device__ __forceinline__ void softmax_update(const float (&sc)[NBK][2][4], int nvalid_last,
-                                               float sl2, float (&m)[NR], float (&l)[NR],
-                                               float (&o)[NR][D / 16][4],
+                                               const float (&sl2)[NR], float (&m)[NR],
+                                               float (&l)[NR], float (&o)[NR][D / 16][4],
                                                float (&pr)[NBK][NR][4], int lane)
 {
     const int t = lane & 3;
@@ -373,10 +378,10 @@ __device__ __forceinline__ void softmax_update(const float (&sc)[NBK][2][4], int
     for (int j = 0; j < NBK; ++j) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-            x[j][r][0] = sc[j][0][2 * r] * sl2;
-            x[j][r][1] = sc[j][0][2 * r + 1] * sl2;
-            x[j][r][2] = sc[j][1][2 * r] * sl2;
-            x[j][r][3] = sc[j][1][2 * r + 1] * sl2;
+            x[j][r][0] = sc[j][0][2 * r] * sl2[r];
+            x[j][r][1] = sc[j][0][2 * r + 1] * sl2[r];
+            x[j][r][2] = sc[j][1][2 * r] * sl2[r];
+            x[j][r][3] = sc[j][1][2 * r + 1] * sl2[r];
         }
     }
     if (nvalid_last < kBlock) {
@@ -435,6 +440,7 @@ __device__ __forceinline__ void softmax_update(const float (&sc)[NBK][2][4], int
 template <int D>
 struct QFrag {
     uint32_t a0[D / 16], a1[D / 16], a2[D / 16], a3[D / 16];
+    float qm[2];    // power of two the lane's row (g, g + 8) was divided by (E4M3 keys)
 };
 
 // Scores q.K of the 16 tokens of one bf16 tile: sc[0] tokens 0-7, sc[1]
@@ -583,8 +589,9 @@ __device__ __forceinline__ void pv_fp8(uint32_t vbase, int nvalid, const float (
 // then P.V.
 template <int D, bool FP8, int NBK, int NR>
 __device__ __forceinline__ void attend_tiles(const uint32_t (&kb)[NBK], int nvalid_last,
-                                             const QFrag<D>& qf, float sl2, float (&m)[NR],
-                                             float (&l)[NR], float (&o)[NR][D / 16][4], int lane)
+                                             const QFrag<D>& qf, const float (&sl2)[NR],
+                                             float (&m)[NR], float (&l)[NR],
+                                             float (&o)[NR][D / 16][4], int lane)
 {
     using G = Geom<D, FP8>;
     float sc[NBK][2][4];
@@ -607,8 +614,9 @@ __device__ __forceinline__ void attend_tiles(const uint32_t (&kb)[NBK], int nval
 // stream uses nr (1 or NRK).
 template <int D, bool FP8, int NBK, int NRK>
 __device__ __forceinline__ void attend(int nr, const uint32_t (&kb)[NBK], int nvalid_last,
-                                       const QFrag<D>& qf, float sl2, float (&m)[NRK],
-                                       float (&l)[NRK], float (&o)[NRK][D / 16][4], int lane)
+                                       const QFrag<D>& qf, const float (&sl2)[NRK],
+                                       float (&m)[NRK], float (&l)[NRK],
+                                       float (&o)[NRK][D / 16][4], int lane)
 {
     if constexpr (NRK == 2) {
         if (nr == 2) {
@@ -616,7 +624,8 @@ __device__ __forceinline__ void attend(int nr, const uint32_t (&kb)[NBK], int nv
             return;
         }
     }
-    attend_tiles<D, FP8, NBK, 1>(kb, nvalid_last, qf, sl2,
+    attend_tiles<D, FP8, NBK, 1>(kb, nvalid_last, qf,
+                                 *reinterpret_cast<const float(*)[1]>(&sl2[0]),
                                  *reinterpret_cast<float(*)[1]>(&m[0]),
                                  *reinterpret_cast<float(*)[1]>(&l[0]),
                                  *reinterpret_cast<float(*)[1][D / 16][4]>(&o[0]), lane);
@@ -627,24 +636,57 @@ __device__ __forceinline__ void attend(int nr, const uint32_t (&kb)[NBK], int nv
 // 16k + 2t + 1), b elements (16k + 8 + 2t, ...); E4M3 keys (f16 operands):
 // the four consecutive elements 16k + 4t .. 16k + 4t + 3, in the order
 // the byte-wise key fragments use.
+//
+// f16 holds every bfloat16 value of magnitude 2^-14 .. 65504 exactly but
+// overflows above 65504, so for E4M3 keys a row whose largest |element| is
+// 2^15 or more is first divided by a power of two 2^e that brings it into
+// [2^14, 2^15) (exact), and 2^e is returned so that the row's scores are
+// multiplied by it again with the softmax scale.  Elements below 2^-24 of the
+// (divided) row round to zero in f16: they change a score by less than
+// D * 2^-25 * 448 code units, against a largest term of at least 2^14.
+// bf16 keys take the bf16 query as it is (returns 1).
 template <int D, bool FP8>
-__device__ __forceinline__ void load_q_row(const DecodeParams& p, int s, int head, bool live,
-                                           int lane, uint32_t (&a)[D / 16], uint32_t (&b)[D / 16])
+__device__ __forceinline__ float load_q_row(const DecodeParams& p, int s, int head, bool live,
+                                            int lane, uint32_t (&a)[D / 16],
+                                            uint32_t (&b)[D / 16])
 {
     const int t = lane & 3;
     const uint16_t* qh = p.q + ((size_t)(live ? s : 0) * p.Hq + (live ? head : 0)) * D;
+    if constexpr (!FP8) {
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-        if (!FP8) {
+        for (int k = 0; k < D / 16; ++k) {
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
             a[k] = live ? __ldg(q32 + 8 * k + t) : 0u;
             b[k] = live ? __ldg(q32 + 8 * k + 4 + t) : 0u;
-        } else {
-            uint2 v = make_uint2(0u, 0u);
-            if (live) v = __ldg(reinterpret_cast<const uint2*>(qh + 16 * k + 4 * t));
-            a[k] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));
-            b[k] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));
         }
+        return 1.f;
+    } else {
+        uint2 v[D / 16];
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            v[k] = make_uint2(0u, 0u);
+            if (live) v[k] = __ldg(reinterpret_cast<const uint2*>(qh + 16 * k + 4 * t));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v[k].x)), fabsf(bf16_hi(v[k].x))),
+                                     fmaxf(fabsf(bf16_lo(v[k].y)), fabsf(bf16_hi(v[k].y)))));
+        }
+        // the row's D elements sit in its 4 lanes (t = 0..3)
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+        float down = 1.f, up = 1.f;
+        if (amax >= 32768.f) {
+            // amax = 1.f * 2^(E - 127) with E its biased exponent; e = E - 141
+            // (e <= 113 for a finite amax: both powers are normal floats)
+            const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 141;
+            down = __uint_as_float((uint32_t)(127 - e) << 23);
+            up = __uint_as_float((uint32_t)(127 + e) << 23);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            a[k] = pack_f16x2(bf16_lo(v[k].x) * down, bf16_hi(v[k].x) * down);
+            b[k] = pack_f16x2(bf16_lo(v[k].y) * down, bf16_hi(v[k].y) * down);
+        }
+        return up;
     }
 }
 
@@ -655,10 +697,12 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, bool chunk, int sc
                                        int lane, QFrag<D>& qf)
 {
     const int g = lane >> 2;
+    qf.qm[1] = 1.f;
     if (!chunk) {
-        load_q_row<D, FP8>(p, sc, h * p.G + g, g < p.G, lane, qf.a0, qf.a2);
+        qf.qm[0] = load_q_row<D, FP8>(p, sc, h * p.G + g, g < p.G, lane, qf.a0, qf.a2);
         if constexpr (NR == 2)
-            load_q_row<D, FP8>(p, sc, h * p.G + g + 8, g + 8 < p.G, lane, qf.a1, qf.a3);
+            qf.qm[1] = load_q_row<D, FP8>(p, sc, h * p.G + g + 8, g + 8 < p.G, lane, qf.a1,
+                                          qf.a3);
         return;
     }
 #pragma unroll
@@ -668,8 +712,8 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, bool chunk, int sc
         int s = -1;
         if (row < rows) s = __ldg(p.chunk + (size_t)sc * KV_PREFIX_CHUNK_INTS + 2 + j);
         const bool live = s >= 0 && s < p.B;
-        if (r == 0) load_q_row<D, FP8>(p, s, h * p.G + i, live, lane, qf.a0, qf.a2);
-        else load_q_row<D, FP8>(p, s, h * p.G + i, live, lane, qf.a1, qf.a3);
+        if (r == 0) qf.qm[0] = load_q_row<D, FP8>(p, s, h * p.G + i, live, lane, qf.a0, qf.a2);
+        else qf.qm[1] = load_q_row<D, FP8>(p, s, h * p.G + i, live, lane, qf.a1, qf.a3);
     }
 }
 
@@ -854,6 +898,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
     uint8_t* gbase = smem_raw + (sbase - sraw);
     const uint32_t stage0 = sbase + (uint32_t)(warp * ST * G::STAGE);
     const uint32_t bar0 = sbase + (uint32_t)(G::BAR_OFF + warp * ST * 8);
+    const uint32_t stall_bar = sbase + (uint32_t)(G::STALL_OFF + warp * 8);
     int4* meta = reinterpret_cast<int4*>(gbase + G::META_OFF) + warp * ST;
 
     if (threadIdx.x == 0) {
@@ -875,6 +920,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
     if (lane == 0) {
 #pragma unroll
         for (int st = 0; st < ST; ++st) mbar_init(bar0 + st * 8, 1);
+        if (p.test_stall > 0) mbar_init(stall_bar, 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -1047,15 +1093,21 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
         // tokens.  (Prefix chunk segments take one tile per update: a second
         // inlined copy of their two-row-tile math costs more than it saves.)
         QFrag<D> qf;
+        float sl2r[NR];           // score scale of the lane's rows (g, g + 8)
         float o[NR][D / 16][4];
         float m[NR], l[NR];
         Seg sg;
         sg.pair = -1;
         bool open = false;
         // Wait for unit i in stage `sst`; on time-out flag the error and let the
-        // copies of units [i, issued_end) land before the warp gives up.
+        // copies of units [i, issued_end) land before the warp gives up.  (Test
+        // hook: with test_stall > 0 the first wait of a range is on a barrier
+        // that nothing arrives on, for test_stall clocks; the copies issued
+        // so far are still waited for, on their own barriers, at the full limit.)
         auto wait_unit = [&](int i, int sst, uint32_t phs, int issued_end) -> bool {
-            bool ok = mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
+            bool ok = (p.test_stall > 0 && i == 0)
+                          ? mbar_wait_bounded(stall_bar, 0u, p.test_stall)
+                          : mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
             ok = __all_sync(kFull, ok);
             if (!ok) {
                 if (lane == 0) {
@@ -1096,6 +1148,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                 sg.i0 = i;
                 load_q<D, FP8, NR>(p, sg.chunk, sg.s, sg.h, sg.rows, lane, qf);
 #pragma unroll
+                for (int r = 0; r < NR; ++r) sl2r[r] = FP8 ? p.sl2 * qf.qm[r] : p.sl2;
+#pragma unroll
                 for (int r = 0; r < NR; ++r) {
                     m[r] = -INFINITY;
                     l[r] = 0.f;
@@ -1123,7 +1177,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                 if (own_last && nvalid == rest)
                     append_patch<D, FP8, NR>(p, sg.s, sg.h, id2, L, kb2, kb2 + G::TILE, lane);
                 const uint32_t kbs[2] = {kb, kb2};
-                attend<D, FP8, 2, NR>(sg.nr, kbs, nvalid, qf, p.sl2, m, l, o, lane);
+                attend<D, FP8, 2, NR>(sg.nr, kbs, nvalid, qf, sl2r, m, l, o, lane);
                 sg.last = blk + 1;
                 __syncwarp();
                 if (i + ST < cnt) issue(i + ST, st);
@@ -1138,7 +1192,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
                     if (own_last && nvalid == L - blk * kBlock)
                         append_patch<D, FP8, NR>(p, sg.s, sg.h, mt.w, L, kb, kb + G::TILE, lane);
                     const uint32_t kbs[1] = {kb};
-                    attend<D, FP8, 1, NR>(sg.nr, kbs, nvalid, qf, p.sl2, m, l, o, lane);
+                    attend<D, FP8, 1, NR>(sg.nr, kbs, nvalid, qf, sl2r, m, l, o, lane);
                 }
                 __syncwarp();
                 if (i + ST < cnt) issue(i + ST, st);
@@ -1359,6 +1413,7 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+std::atomic<long long> g_test_stall{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 template <int D, bool FP8, int NR>
@@ -1710,6 +1765,7 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     dp.prow = nr == 2 ? KV_PREFIX_MAX_ROWS : dp.G;
     dp.slot_base = nc > 0 ? warps_total : 0;
     dp.early = pre && (pre->flags & KV_DECODE_EARLY_INPUTS) ? 1 : 0;
+    dp.test_stall = g_test_stall.load(std::memory_order_relaxed);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (ev_begin && cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), st) != cudaSuccess)
@@ -1783,7 +1839,8 @@ int decode_read_error(unsigned* flags, long long* detail)
 // every device loading the library holds until the process exits.  Host code
 // must not use the symbol's name as an address: its device address is looked
 // up once per device with cudaGetSymbolAddress (with that device current).
-constexpr size_t kStaticWorkspaceBytes = 16u << 20;     // 16 MiB
+constexpr size_t kStaticWorkspaceBytes = KV_NOALLOC_WORKSPACE_BYTES;     // 16 MiB
+static_assert(kStaticWorkspaceBytes == (size_t)16 << 20, "the size the header promises");
 __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
 
 namespace {
@@ -1858,6 +1915,53 @@ extern "C" int paged_decode(void* out, int out_dtype, const void* q, const void*
                          num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
                          stream, k_new ? &app : nullptr, &pre, nullptr, nullptr, nullptr);
+}
+
+extern "C" int paged_decode_timed(void* out, int out_dtype, const void* q, const void* k_new,
+                                  const void* v_new, void* k_cache, void* v_cache, int kv_dtype,
+                                  float k_scale, float v_scale, int num_blocks,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, float scale,
+                                  const int32_t* chunks, const int32_t* seq_chunk,
+                                  int num_chunks, unsigned flags, void* workspace,
+                                  size_t workspace_bytes, void* stream, void* ev_begin,
+                                  void* ev_split_end, void* ev_end)
+{
+    if ((k_new == nullptr) != (v_new == nullptr)) return KV_ERR_INVALID_ARG;
+    if (flags & ~KV_DECODE_EARLY_INPUTS) return KV_ERR_INVALID_ARG;
+    const AppendArgs app = {k_new, v_new, k_cache, v_cache};
+    const PrefixArgs pre = {chunks, seq_chunk, num_chunks, flags};
+    return decode_launch(out, out_dtype, q, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                         num_blocks, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, scale, workspace, workspace_bytes,
+                         stream, k_new ? &app : nullptr, &pre, ev_begin, ev_split_end, ev_end);
+}
+
+extern "C" int kv_prefix_plan(const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int kv_dtype, int resident_warps,
+                              int32_t* chunks, int32_t* seq_chunk, int* num_chunks)
+{
+    if (!num_chunks) return KV_ERR_INVALID_ARG;
+    *num_chunks = 0;
+    if (int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, kv_dtype)) return rc;
+    if (resident_warps <= 0) {
+        // the plain split kernel's persistent grid on the current device
+        int sms = 0, cps = 0;
+        if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, 1, sms, cps)) return rc;
+        resident_warps = sms * cps * kWarps;
+    }
+    return prefix_plan_host(block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                            num_q_heads / num_kv_heads, num_kv_heads, resident_warps, chunks,
+                            seq_chunk, num_chunks);
+}
+
+extern "C" int kv_test_pipeline_stall(long long cycles)
+{
+    if (cycles < 0 || cycles > kWaitLimit) return KV_ERR_INVALID_ARG;
+    g_test_stall.store(cycles, std::memory_order_relaxed);
+    return KV_OK;
 }
 
 extern "C" int paged_decode_attention_timed(

@@ -568,6 +568,42 @@ def test_bad_inputs_are_flagged_not_faulted():
     assert float(x.sum()) == 8.0
 
 
+@pytest.mark.parametrize("prefix", [False, True], ids=["plain", "prefix_chunks"])
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, prefix):
+    """The bounded wait on a bulk copy: with the test hook every warp's first
+    wait is on a barrier that nothing arrives on (no copy is lost -- the
+    copies it issued are still waited for before it stops).  The time-out
+    must raise KV_DEVERR_PIPELINE_TIMEOUT (and nothing else), and the next
+    call on the same context must give the oracle's result."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(6, 32, 8, 128, [1, 17, 300, 4097, 2000, 33],
+                                 kv_dtype=kv_dtype, seed=93)
+    pre = None
+    if prefix:
+        case = workloads.make_case("3", override={"B": 16, "N_hi": 3000, "kv_dtype": kv_dtype},
+                                   seed=94)
+        pre = pk.prefix_chunks(case.block_tables, case.context_lens, case.G)
+        assert len(pre[0]) > 0
+    pk.get_device_error()
+    pk.set_pipeline_stall(20000)                 # ~10 us of SM clocks
+    try:
+        H.gpu_step(case, fused=True, early_inputs=True, prefix=pre)
+    finally:
+        pk.set_pipeline_stall(0)
+    flags, detail = pk.get_device_error()
+    assert flags == pk.DEVERR_PIPELINE_TIMEOUT and detail == 0, (flags, detail)
+    x = torch.ones(4, device="cuda") * 2
+    assert float(x.sum()) == 8.0
+    out, kc, vc = H.gpu_step(case, fused=True, early_inputs=True, prefix=pre)
+    okc, ovc = H.oracle_caches(case)
+    assert np.array_equal(cache_bits(kc), okc) and np.array_equal(cache_bits(vc), ovc)
+    H.compare(case, out, H.oracle_step(case, okc, ovc), what="after a time-out")
+    assert pk.get_device_error()[0] == 0
+    with pytest.raises(pk.KVError):
+        pk.set_pipeline_stall(-1)
+
+
 def test_context_longer_than_its_table_row_is_flagged_and_clamped():
     """A context length past its block-table row (the context-limit overflow
     case) or below zero is reported as KV_DEVERR_CONTEXT_TOO_LONG with the bad

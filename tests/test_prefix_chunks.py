@@ -165,3 +165,44 @@ def test_random_prefix_trees_obey_every_rule(pk, seed):
     for row in chunks:
         members = [int(x) for x in row[2:2 + int(row[1])]]
         assert len({int(group_of[s]) for s in members}) == 1
+
+
+def _saved_fraction(chunks, lens):
+    saved = sum(int(r[0]) * (int(r[1]) - 1) for r in chunks)
+    return saved / float((-(-np.asarray(lens, dtype=np.int64) // 16)).sum())
+
+
+@pytest.mark.parametrize("cfg,override,want_chunks", [
+    ("3", None, False),                 # 608-token prompt: ~5 % of the blocks saved
+    ("3L", None, True),                 # 4096-token prompt: about half saved
+    ("3L", {"B": 32}, False),           # 256 pairs: fewer than the resident warps
+    ("3L", {"B": 256, "prefix_blocks": 64}, True),
+    ("3L", {"B": 256, "prefix_blocks": 16}, False),
+])
+def test_plan_uses_chunks_only_where_they_pay(pk, cfg, override, want_chunks):
+    """kv_prefix_plan keeps kv_prefix_chunks' table when it saves >= 6 % of
+    the blocks read and the step has more (sequence, KV head) pairs than the
+    1216 resident warps of a GB300 (152 SMs x 2 CTAs x 4 warps); otherwise it
+    asks for plain decoding (no chunks, seq_chunk all -1)."""
+    spec, L, bt, NB, _, _ = workloads.make_layout(cfg, override=override)
+    G = spec["Hq"] // spec["Hkv"]
+    full = pk.prefix_chunks(bt, L, G)
+    chunks, seq_chunk = pk.prefix_plan(bt, L, spec["Hq"], spec["Hkv"], spec["D"],
+                                       resident_warps=1216)
+    frac = _saved_fraction(full[0], L)
+    pays = frac >= 0.06 and spec["B"] * spec["Hkv"] > 1216
+    assert pays == want_chunks, frac
+    if want_chunks:
+        np.testing.assert_array_equal(chunks, full[0])
+        np.testing.assert_array_equal(seq_chunk, full[1])
+        check_table(bt, L, G, chunks, seq_chunk)
+    else:
+        assert len(full[0]) > 0 and len(chunks) == 0 and (seq_chunk == -1).all()
+
+
+def test_plan_refuses_large_groups_and_bad_shapes(pk):
+    spec, L, bt, NB, _, _ = workloads.make_layout("3L")
+    chunks, seq_chunk = pk.prefix_plan(bt, L, 256, 8, 128, resident_warps=1216)   # G = 32
+    assert len(chunks) == 0 and (seq_chunk == -1).all()
+    with pytest.raises(pk.KVError):
+        pk.prefix_plan(bt, L, 30, 8, 128, resident_warps=1216)                   # Hq % Hkv

@@ -153,20 +153,18 @@ def _layout(rng, nblocks, B, shared=None, slack=0.10, pool_blocks=None, max_bloc
     return bt, pool_blocks, nshared.astype(np.int32)
 
 
-def make_case(cfg, device="cpu", seed=None, override=None):
-    """Build the seeded decode-step inputs of configuration ``cfg``.
-
-    ``override`` replaces recipe entries (used by tests to shrink a config
-    while keeping its structure, e.g. ``{"B": 4}``)."""
+def make_layout(cfg, seed=None, override=None):
+    """The lengths and block placement of configuration ``cfg`` alone (no
+    values): (spec, context lengths after the append, block tables, pool
+    blocks, shared blocks per sequence, seed) -- the same tables make_case
+    builds for the same arguments."""
     spec = dict(CONFIGS[cfg])
     if override:
         spec.update(override)
     if seed is None:
         seed = SEED_BASE + SEED_OFFSET[cfg]
     rng = np.random.default_rng(seed)
-    gen = _gen(device, seed)
-    B, Hq, Hkv, D = spec["B"], spec["Hq"], spec["Hkv"], spec["D"]
-
+    B = spec["B"]
     if "N" in spec:
         N = np.full(B, spec["N"], dtype=np.int64)
     else:
@@ -185,6 +183,17 @@ def make_case(cfg, device="cpu", seed=None, override=None):
         shared = (group_of, nshared, spec["prefix_blocks"])
     bt, NB, nshared = _layout(rng, nblocks, B, shared, spec.get("slack", 0.10),
                               spec.get("pool_blocks"), spec.get("max_blocks"))
+    return spec, L, bt, NB, nshared, seed
+
+
+def make_case(cfg, device="cpu", seed=None, override=None):
+    """Build the seeded decode-step inputs of configuration ``cfg``.
+
+    ``override`` replaces recipe entries (used by tests to shrink a config
+    while keeping its structure, e.g. ``{"B": 4}``)."""
+    spec, L, bt, NB, nshared, seed = make_layout(cfg, seed, override)
+    gen = _gen(device, seed)
+    B, Hq, Hkv, D = spec["B"], spec["Hq"], spec["Hkv"], spec["D"]
 
     q = _randn_bf16((B, Hq, D), gen, device)
     k_new = _randn_bf16((B, Hkv, D), gen, device)
