@@ -1100,27 +1100,30 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
         sg.pair = -1;
         bool open = false;
         // Wait for unit i in stage `sst`; on time-out flag the error and let the
-        // copies of units [i, issued_end) land before the warp gives up.  (Test
-        // hook: with test_stall > 0 the first wait of a range is on a barrier
-        // that nothing arrives on, for test_stall clocks; the copies issued
-        // so far are still waited for, on their own barriers, at the full limit.)
-        auto wait_unit = [&](int i, int sst, uint32_t phs, int issued_end) -> bool {
-            bool ok = (p.test_stall > 0 && i == 0)
-                          ? mbar_wait_bounded(stall_bar, 0u, p.test_stall)
-                          : mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
-            ok = __all_sync(kFull, ok);
-            if (!ok) {
-                if (lane == 0) {
-                    raise_flag(&g_decode_err, KV_DEVERR_PIPELINE_TIMEOUT, i);
-                    for (int j = i; j < issued_end; ++j) {
-                        mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
-                        if (++sst == ST) { sst = 0; phs ^= 1u; }
-                    }
+        // copies of units [i, issued_end) land before the warp gives up.
+        auto give_up = [&](int i, int sst, uint32_t phs, int issued_end) {
+            if (lane == 0) {
+                raise_flag(&g_decode_err, KV_DEVERR_PIPELINE_TIMEOUT, i);
+                for (int j = i; j < issued_end; ++j) {
+                    mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit);
+                    if (++sst == ST) { sst = 0; phs ^= 1u; }
                 }
-                __syncwarp();
             }
+            __syncwarp();
+        };
+        auto wait_unit = [&](int i, int sst, uint32_t phs, int issued_end) -> bool {
+            const bool ok = __all_sync(kFull, mbar_wait_bounded(bar0 + sst * 8, phs, kWaitLimit));
+            if (!ok) give_up(i, sst, phs, issued_end);
             return ok;
         };
+        // Test hook: a first wait on a barrier that nothing arrives on, for
+        // test_stall clocks; the copies issued so far are still waited for,
+        // on their own barriers, at the full limit.
+        if (p.test_stall > 0 &&
+            !__all_sync(kFull, mbar_wait_bounded(stall_bar, 0u, p.test_stall))) {
+            give_up(0, st, phase, min(cnt, ST));
+            return;
+        }
         for (int i = 0; i < cnt;) {
             const int issued_end = min(cnt, i + ST);
             if (!wait_unit(i, st, phase, issued_end)) return;
