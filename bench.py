@@ -41,11 +41,11 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "33345e5c784bf22118c7bf7d5bd09e4004317648a09aa9b5b4c96fac18439cb7",
-           "bytes_per_launch": 1088765952,
+TRAFFIC = {"kernel_sha256": "6f8b70001de92aab6e2bd34fbce919d6ab769d95aeb283588146fdc518d1b949",
+           "bytes_per_launch": 1087719424,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,145,344 B + 3,046,144 B), scaled x4 by units processed "
-                     "(profiles/paged_decode_split_b8_full.md)"}
+                     "(269,149,440 B + 2,780,416 B), scaled x4 by units processed "
+                     "(profiles/smem_bank_conflicts_split_b8.md)"}
 
 
 def parse_args(argv=None):
