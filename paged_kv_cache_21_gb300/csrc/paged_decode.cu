@@ -70,6 +70,7 @@
 #include "device_common.cuh"
 #include "internal.h"
 #include "paged_kv.h"
+#include "wide.h"
 
 namespace pkv {
 
@@ -1615,9 +1616,24 @@ int check_shape(int num_seqs, int Hq, int Hkv, int D, int kv_dtype)
 // slots (a second set of per-warp slots for the prefix-chunk phase).
 struct LaunchPlan {
     HeadSplit hs;
+    bool wide;             // the tensor-memory kernel for groups above 16 rows
     int nr, grid, warps_total, slot_warps;
     WsLayout ws;
 };
+
+// Groups of more than 64 query rows per KV head on a bf16 cache with
+// head_dim 128 run the wide-group kernel (5th-generation tensor cores, all
+// rows of a group in one 128-row MMA); it writes its partials in the
+// sub-group layout below, so the same merge kernel follows.  Measured on
+// GB300 (32 sequences x 8193 tokens, one KV head): 128 rows 71.6 us against
+// 108.9 us for the sub-group kernel; at 64 rows the two tie (61.6 us) and
+// below it the sub-group kernel is faster (32 rows: 38.5 against 56-58 us).
+constexpr int kWideMinRows = 65;
+
+bool use_wide(int Hq, int Hkv, int D, bool fp8, int nc)
+{
+    return !fp8 && D == 128 && nc == 0 && Hq / Hkv >= kWideMinRows;
+}
 
 int plan_launch(int B, int nc, int Hq, int Hkv, int D, bool fp8, LaunchPlan& lp)
 {
@@ -1625,7 +1641,19 @@ int plan_launch(int B, int nc, int Hq, int Hkv, int D, bool fp8, LaunchPlan& lp)
     // prefix chunks pack at least two members' rows into 16: G <= 8
     if (nc > 0 && 2 * (Hq / Hkv) > KV_PREFIX_MAX_ROWS) return KV_ERR_UNSUPPORTED;
     lp.nr = (nc > 0 || lp.hs.G_v > 8) ? 2 : 1;
+    lp.wide = use_wide(Hq, Hkv, D, fp8, nc);
     int sms = 0, cps = 0;
+    if (lp.wide) {
+        // partial slots of one sub-group: one per (sequence, KV head) plus
+        // one per CTA (a CTA's partial of pair x goes to slot x + CTA)
+        sms = num_sms_current();
+        if (int rc = wide_setup(cps)) return rc;
+        lp.grid = sms * cps;
+        lp.warps_total = lp.grid;
+        lp.slot_warps = lp.grid << lp.hs.hshift;
+        lp.ws = ws_layout(B, 0, Hq, lp.hs.Hkv_v, D, lp.slot_warps, 2);
+        return KV_OK;
+    }
     if (int rc = device_info(D, fp8, lp.nr, sms, cps)) return rc;
     lp.grid = sms * cps;
     lp.warps_total = lp.grid * kWarps;
@@ -1774,12 +1802,41 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     if (ev_begin && cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), st) != cudaSuccess)
         return KV_ERR_CUDA;
     cudaError_t err;
-    if (head_dim == 128)
+    if (lp.wide) {
+        WideParams wp;
+        wp.q = dp.q;
+        wp.out = out;
+        wp.bt = block_tables;
+        wp.ctx = context_lens;
+        wp.part_o = dp.part_o;
+        wp.part_ml = dp.part_ml;
+        wp.pair_meta = dp.pair_meta;
+        wp.k_new = dp.k_new;
+        wp.v_new = dp.v_new;
+        wp.k_cache = dp.k_cache;
+        wp.v_cache = dp.v_cache;
+        wp.B = num_seqs;
+        wp.Hq = num_q_heads;
+        wp.Hkv_p = num_kv_heads;
+        wp.G = num_q_heads / num_kv_heads;
+        wp.Gv = lp.hs.G_v;
+        wp.hshift = lp.hs.hshift;
+        wp.max_blocks = max_blocks_per_seq;
+        wp.num_blocks = num_blocks;
+        wp.nctas = grid;
+        wp.min_q = dp.min_q1;
+        wp.team_slots = num_seqs * num_kv_heads + grid;
+        wp.sl2 = dp.sl2;
+        wp.out_f32 = dp.out_f32;
+        wp.early = dp.early;
+        err = wide_launch(mk, mv, wp, st);
+    } else if (head_dim == 128) {
         err = fp8 ? launch_split<128, true>(nr, grid, st, mk, mv, dp)
                   : launch_split<128, false>(nr, grid, st, mk, mv, dp);
-    else
+    } else {
         err = fp8 ? launch_split<64, true>(nr, grid, st, mk, mv, dp)
                   : launch_split<64, false>(nr, grid, st, mk, mv, dp);
+    }
     if (err != cudaSuccess) return KV_ERR_CUDA;
     if (ev_split && cudaEventRecord(static_cast<cudaEvent_t>(ev_split), st) != cudaSuccess)
         return KV_ERR_CUDA;
@@ -2011,12 +2068,13 @@ extern "C" int paged_decode_step(void* out, int out_dtype, const void* q, const 
 
 extern "C" int kv_get_device_error(int* flags, int64_t* detail)
 {
-    unsigned f1 = 0, f2 = 0;
-    long long d1 = -1, d2 = -1;
+    unsigned f1 = 0, f2 = 0, f3 = 0;
+    long long d1 = -1, d2 = -1, d3 = -1;
     if (int rc = append_read_error(&f1, &d1)) return rc;
     if (int rc = decode_read_error(&f2, &d2)) return rc;
-    if (flags) *flags = (int)(f1 | f2);
-    if (detail) *detail = f1 ? d1 : d2;
+    if (int rc = wide_read_error(&f3, &d3)) return rc;
+    if (flags) *flags = (int)(f1 | f2 | f3);
+    if (detail) *detail = f1 ? d1 : (f2 ? d2 : d3);
     return KV_OK;
 }
 

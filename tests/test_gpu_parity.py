@@ -238,13 +238,15 @@ LARGE_GROUP_LENS = [1, 17, 300, 4097, 2000, 33]
 
 @pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
 @pytest.mark.parametrize("Hq,Hkv,D", [(12, 1, 128), (16, 2, 128), (24, 3, 128), (32, 1, 128),
-                                      (48, 2, 64), (64, 1, 128), (128, 1, 64)])
+                                      (48, 2, 64), (64, 1, 128), (128, 1, 64), (128, 1, 128),
+                                      (256, 2, 128), (80, 1, 128), (96, 1, 128), (72, 1, 128)])
 def test_large_query_groups(Hq, Hkv, D, kv_dtype):
     """G = 12..128, MQA on many-head models ("KV cache complete guide",
     section "(2) GQA": one KV head for all query heads): 9-16 rows run the
     two-row-tile kernel, larger groups run as 2, 4 or 8 sub-groups that read
-    the same KV tiles.  Two-launch and fused paths, float32 output, and the
-    append written by every sub-group lands once, bit-exact."""
+    the same KV tiles, and above 64 rows (bf16, d128) the tensor-memory
+    kernel takes the whole group in one 128-row MMA.  Two-launch and fused
+    paths, float32 output, and the append lands once, bit-exact."""
     case = workloads.make_custom(len(LARGE_GROUP_LENS), Hq, Hkv, D, LARGE_GROUP_LENS,
                                  kv_dtype=kv_dtype, seed=Hq + Hkv)
     what = "Hq%d Hkv%d D%d dt%d" % (Hq, Hkv, D, kv_dtype)
@@ -253,7 +255,7 @@ def test_large_query_groups(Hq, Hkv, D, kv_dtype):
     check_case(case, what="f32 " + what, out_dtype=torch.float32)
 
 
-@pytest.mark.parametrize("Hq", [32, 64])
+@pytest.mark.parametrize("Hq", [32, 64, 128])
 def test_mqa_full_size_and_deterministic(Hq):
     """One KV head for Hq query heads at the 8B layer's batch and context
     (32 sequences x 8193 tokens, d128): every output against the oracle, and
@@ -266,6 +268,37 @@ def test_mqa_full_size_and_deterministic(Hq):
     o2, _, _ = H.gpu_step(case, fused=True, early_inputs=True)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert pk.get_device_error()[0] == 0
+
+
+@pytest.mark.parametrize("lens", [[100000], [30000, 1, 17, 20000]])
+def test_wide_groups_split_over_many_ctas(lens):
+    """128 query rows on one KV head with pairs cut across tens of CTAs of
+    the tensor-memory kernel (partials in sub-groups of 16 rows, then the
+    merge), short pairs seen whole by one CTA beside them."""
+    case = workloads.make_custom(len(lens), 128, 1, 128, lens, seed=len(lens) + 77)
+    check_case(case, what="wide %s" % lens, fused=True, early_inputs=True)
+    check_case(case, what="wide f32 %s" % lens, out_dtype=torch.float32)
+
+
+def test_wide_groups_flag_bad_block_ids():
+    """A block id outside the pool in the tensor-memory kernel is not
+    fetched: its keys are masked, KV_DEVERR_BLOCK_OUT_OF_RANGE is raised with
+    the id, nothing faults and the rest of the batch is unaffected."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(3, 128, 1, 128, [40, 300, 700], seed=91)
+    out_ok, kc, vc = H.gpu_step(case, out_dtype=torch.float32)
+    pk.get_device_error()
+    bt = torch.from_numpy(case.block_tables).cuda()
+    bad = bt.clone()
+    bad[1, 3] = case.num_blocks + 11
+    out = torch.empty_like(out_ok)
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    pk.paged_decode_attention(out, case.q.cuda(), kc, vc, bad,
+                              torch.from_numpy(case.context_lens).cuda(), case.scale, ws)
+    torch.cuda.synchronize()
+    assert pk.get_device_error() == (pk.DEVERR_BLOCK_OUT_OF_RANGE, case.num_blocks + 11)
+    assert torch.isfinite(out).all()
+    assert torch.equal(out[0], out_ok[0]) and torch.equal(out[2], out_ok[2])
 
 
 def test_prefix_chunks_refuse_groups_above_eight():
@@ -297,7 +330,7 @@ def test_many_sequences_beyond_register_scan(Hq, Hkv):
     check_case(case, what="B=700 fused", fused=True)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 1), (64, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 1), (64, 2), (128, 1)])
 def test_empty_contexts_give_zeros(Hq, Hkv):
     lens = [0, 33, 0, 1, 0]
     case = workloads.make_custom(5, Hq, Hkv, 128, [max(x, 1) for x in lens], seed=4)
@@ -313,7 +346,7 @@ def test_empty_contexts_give_zeros(Hq, Hkv):
     assert err < 2e-3
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (48, 1)])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (48, 1), (128, 1)])
 def test_nan_canaries_in_unused_slots_are_never_read(Hq, Hkv):
     case = workloads.make_custom(4, Hq, Hkv, 128, [1, 18, 333, 1000], seed=8, slack=0.5)
     used = np.zeros(case.num_blocks * 16, dtype=bool)
