@@ -1621,14 +1621,14 @@ struct LaunchPlan {
     WsLayout ws;
 };
 
-// Groups of more than 64 query rows per KV head on a bf16 cache with
-// head_dim 128 run the wide-group kernel (5th-generation tensor cores, all
-// rows of a group in one 128-row MMA); it writes its partials in the
-// sub-group layout below, so the same merge kernel follows.  Measured on
-// GB300 (32 sequences x 8193 tokens, one KV head): 128 rows 71.6 us against
-// 108.9 us for the sub-group kernel; at 64 rows the two tie (61.6 us) and
-// below it the sub-group kernel is faster (32 rows: 38.5 against 56-58 us).
-constexpr int kWideMinRows = 65;
+// Groups of 64 or more query rows per KV head on a bf16 cache with head_dim
+// 128 run the wide-group kernel (5th-generation tensor cores, all rows of a
+// group in one 128-row MMA); it writes its partials in the sub-group layout
+// below, so the same merge kernel follows.  Measured on GB300 (32 sequences
+// x 8193 tokens, one KV head, fused step): 128 rows 63.6 us against 108.9 us
+// for the sub-group kernel, 64 rows 54.1 against 61.5; at 32 rows the
+// sub-group kernel is faster (38.4 against 49.4 us).
+constexpr int kWideMinRows = 64;
 
 bool use_wide(int Hq, int Hkv, int D, bool fp8, int nc)
 {

@@ -23,8 +23,8 @@
 //    K and V tiles of its units into a 9-stage ring with TMA (the split
 //    kernel's tensor maps, 128-byte swizzle; the K tiles of consecutive
 //    stages form one contiguous operand) and does the fused append; warp 5
-//    allocates tensor memory and issues the MMAs; warps 0-3 own one query row
-//    per thread (softmax and output).
+//    allocates tensor memory and issues the score MMAs, warp 6 the P.V MMAs;
+//    warps 0-3 own one query row per thread (softmax and output).
 //  * Units are consumed in chunks of up to 4 blocks of one (sequence, head)
 //    pair.  S = Q K^T: M = 128 query rows (the group, padded), N = 16 keys
 //    per block of the chunk in one MMA per 16-wide k-step, K = 128, f32 in
@@ -32,7 +32,7 @@
 //    applies the length mask, keeps a reference maximum that moves only when
 //    the chunk maximum exceeds it by more than 2^8 (then the accumulator row
 //    is rescaled in tensor memory), and stores P = 2^(x - m) split into bf16
-//    high and low parts in tensor memory.  O += P_hi V + P_lo V (A from
+//    high and low parts in tensor memory, over the chunk's S.  O += P_hi V + P_lo V (A from
 //    tensor memory, V as an MN-major operand straight from the ring), f32 in
 //    tensor memory.  The MMA warp computes the next chunk's scores while the
 //    row threads work on this one.
@@ -62,12 +62,8 @@ namespace {
 
 constexpr int D = 128;
 constexpr int kRows = 128;                      // M of every MMA
-#ifndef PKV_WIDE_CHUNK
-#define PKV_WIDE_CHUNK 4
-#endif
-constexpr int kChunk = PKV_WIDE_CHUNK;          // blocks per chunk
+constexpr int kChunk = 4;                       // blocks per chunk
 constexpr int kKeys = kChunk * kBlock;          // keys per chunk (S columns)
-static_assert(kKeys == 32 || kKeys == 64, "chunks of 2 or 4 blocks");
 constexpr int kStages = 9;                      // ring stages (one block's K and V)
 constexpr int kBox = kBlock * 128;              // one box: 16 rows x 128 bytes
 constexpr int kRegion = kRows * 128;            // 128 rows x 128 bytes
@@ -81,27 +77,31 @@ enum Bar {
     B_EMPTY = kStages,           // + stage: the MMAs reading them are done
     B_PATCH = 2 * kStages,       // + stage: the copy warp has edited the tiles
     B_QFULL = 3 * kStages,       // Q of the next segment is in place
-    B_INFO,                      // + buffer: the chunk description is written
-    B_INFO1,
-    B_SFULL,                     // S computed
-    B_SFREE,                     // S read by the row threads
-    B_PFULL,                     // P written
-    B_PVDONE,                    // the chunk's P.V MMAs are done
+    B_INFO,                      // + entry (4): the chunk description is written
+    B_INFOFREE = B_INFO + 4,     // + entry (4): the P.V warp has read it
+    B_SFULL = B_INFOFREE + 4,    // + buffer: S computed
+    B_SFULL1,
+    B_PFULL,                     // + buffer: P written
+    B_PFULL1,
+    B_PVDONE,                    // + buffer: the P.V MMAs reading that P are done
+    B_PVDONE1,
     B_OFULL,                     // the segment's accumulator is complete
     B_OFREE,                     // the row threads have read it
-    B_FINAL,                     // every MMA of the CTA is done
+    B_FINAL_S,                   // every score MMA of the CTA is done
+    B_FINAL_PV,                  // every P.V MMA of the CTA is done
     kNumBars
 };
 constexpr int kMetaOff = kBarOff + (kNumBars * 8 + 15) / 16 * 16;
-constexpr int kInfoOff = kMetaOff + kStages * 16;     // 2 buffers x 2 int4
-constexpr int kMiscOff = kInfoOff + 2 * 32;
+constexpr int kInfoOff = kMetaOff + kStages * 16;     // 4 entries x 2 int4
+constexpr int kMiscOff = kInfoOff + 4 * 32;
 constexpr int kSmem = kMiscOff + 64 + 1024;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;                  // S: columns 0-63
-constexpr uint32_t kColPhi = 64;               // P high parts: up to 32 columns (64 bf16)
-constexpr uint32_t kColPlo = 96;               // P low parts
-constexpr uint32_t kColO = 128;                // O: columns 128-255
-constexpr int kThreads = 192;
+// tensor memory: buffer b at columns 64b holds S of a chunk (64 keys, f32),
+// then, in place, its P (32 columns of bf16 pairs for the high parts, then 32
+// for the low parts); O at columns 128-255
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;
+constexpr int kThreads = 224;                   // 7 warps
 constexpr long long kWaitLimit = 1LL << 31;    // ~1 s of SM clocks
 constexpr uint32_t kIdescPV = umma::idesc_bf16_f32(kRows, D, false, true);
 static_assert(kSmem <= 232448 / 2 - 1024, "two CTAs per SM");
@@ -249,15 +249,19 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
             mbar_init(bar(B_PATCH + s), 1);
         }
         mbar_init(bar(B_QFULL), nact);
-        mbar_init(bar(B_INFO), 1);
-        mbar_init(bar(B_INFO1), 1);
-        mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_SFREE), nact);
-        mbar_init(bar(B_PFULL), nact);
-        mbar_init(bar(B_PVDONE), 1);
+        for (int e = 0; e < 4; ++e) {
+            mbar_init(bar(B_INFO + e), 1);
+            mbar_init(bar(B_INFOFREE + e), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_SFULL + b), 1);
+            mbar_init(bar(B_PFULL + b), nact);
+            mbar_init(bar(B_PVDONE + b), 1);
+        }
         mbar_init(bar(B_OFULL), 1);
         mbar_init(bar(B_OFREE), nact);
-        mbar_init(bar(B_FINAL), 1);
+        mbar_init(bar(B_FINAL_S), 1);
+        mbar_init(bar(B_FINAL_PV), 1);
         misc[M_ABORT] = 0;
         fence_mbar_init();
     }
@@ -364,20 +368,23 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int nvalid = L - j * kBlock;
             const bool fix = !valid || (j == nb - 1 && (append || nvalid < kBlock));
             const uint32_t kst = sb + kKOff, vst = sb + kVOff;
+            const uint32_t fb = bar(B_FULL + st);
             if (lane == 0) {
                 meta[st] = make_int4(s * p.Hkv_p + h, j, L, (valid ? 1 : 0) | (fix ? 2 : 0));
                 if (valid) {
-                    const uint32_t fb = bar(B_FULL + st);
                     mbar_arrive_expect_tx(fb, (uint32_t)(4 * kBox));
-                    const int z = id * p.Hkv_p + h;
-                    tma_load_3d_hint(kst + st * kBox, &tm_k, 0, 0, z, fb, pol);
-                    tma_load_3d_hint(kst + kRingRegion + st * kBox, &tm_k, 64, 0, z, fb, pol);
-                    tma_load_3d_hint(vst + st * kBox, &tm_v, 0, 0, z, fb, pol);
-                    tma_load_3d_hint(vst + kRingRegion + st * kBox, &tm_v, 64, 0, z, fb, pol);
                 } else {
                     raise_flag(&g_wide_err, KV_DEVERR_BLOCK_OUT_OF_RANGE, id);
-                    mbar_arrive(bar(B_FULL + st));
+                    mbar_arrive(fb);
                 }
+            }
+            __syncwarp();
+            // the four boxes of the unit (K and V, d 0-63 and 64-127) are issued
+            // by four lanes in one instruction
+            if (valid && lane < 4) {
+                const int z = id * p.Hkv_p + h;
+                const uint32_t dst = (lane < 2 ? kst : vst) + (uint32_t)((lane & 1) * kRingRegion + st * kBox);
+                tma_load_3d_hint(dst, lane < 2 ? &tm_k : &tm_v, (lane & 1) * 64, 0, z, fb, pol);
             }
             issued = i + 1;
             if (fix) {
@@ -431,11 +438,13 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
             // descriptors of the operands' first atoms (start fields advance below)
             const uint64_t qdesc0 = umma::smem_desc_sw128(sb + kQOff, 16, 1024);
             const uint64_t kdesc0 = umma::smem_desc_sw128(sb + kKOff, 16, 1024);
-            const uint64_t vdesc0 = umma::smem_desc_sw128(sb + kVOff, kRingRegion, 1024);
             int seg = -1;
             bool prev_end = true;
             // wait for a chunk's tiles (and edits), describe it to the row threads
             auto plan = [&](int i, int k, ChunkInfo& c) -> bool {
+                // entry k & 3 last described chunk k - 4: the P.V warp must be done with it
+                if (k >= 4 && !wait_bar(bar(B_INFOFREE + (k & 3)), (uint32_t)(((k - 4) >> 2) & 1), misc))
+                    return false;
                 const int st = i % kStages;
                 if (!wait_bar(bar(B_FULL + st), (uint32_t)((i / kStages) & 1), misc)) return false;
                 const int4 m0 = meta[st];
@@ -463,12 +472,15 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 c.a = make_int4(i, n, m0.x, m0.y);
                 c.b = make_int4(m0.z, vmask, (start ? 1 : 0) | (end ? 2 : 0), seg);
-                info[k & 1] = c;
-                mbar_arrive(bar(B_INFO + (k & 1)));
+                info[k & 3] = c;
+                mbar_arrive(bar(B_INFO + (k & 3)));
                 return true;
             };
             auto issue_s = [&](const ChunkInfo& c, int k) -> bool {
-                if (k >= 1 && !wait_bar(bar(B_SFREE), (uint32_t)((k - 1) & 1), misc)) return false;
+                const int b = k & 1;
+                // buffer b holds P of chunk k - 2 until its P.V products are done
+                if (k >= 2 && !wait_bar(bar(B_PVDONE + b), (uint32_t)(((k - 2) >> 1) & 1), misc))
+                    return false;
                 if ((c.b.z & 1) && !wait_bar(bar(B_QFULL), (uint32_t)(c.b.w & 1), misc))
                     return false;
                 umma::fence_after_sync();
@@ -480,7 +492,7 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const int np = part == 0 ? n0 : n - n0;
                     if (np <= 0) break;
                     const int sp = part == 0 ? s0 : 0;
-                    const uint32_t d = tmem + kColS + (uint32_t)(16 * (part == 0 ? 0 : n0));
+                    const uint32_t d = tmem + kColS + (uint32_t)(64 * b + 16 * (part == 0 ? 0 : n0));
                     const uint32_t idesc = umma::idesc_bf16_f32(kRows, 16 * np, false, false);
                     const uint64_t bd0 = kdesc0 + (uint64_t)((sp * kBox) >> 4);
 #pragma unroll
@@ -492,44 +504,57 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                         umma::mma_bf16_ss(d, a, bd, idesc, kk > 0);
                     }
                 }
-                umma::commit(bar(B_SFULL));
+                umma::commit(bar(B_SFULL + b));
                 return true;
             };
-            auto issue_pv = [&](const ChunkInfo& c, int k) -> bool {
-                if (!wait_bar(bar(B_PFULL), (uint32_t)(k & 1), misc)) return false;
+            // the score MMAs of this warp run up to two chunks ahead of the
+            // row threads; warp 6 issues the P.V products
+            ChunkInfo c;
+            int next_i = 0;
+            bool ok = true;
+            for (int k = 0; ok && next_i < cnt; ++k) {
+                ok = plan(next_i, k, c) && issue_s(c, k);
+                next_i = c.a.x + c.a.y;
+            }
+            // every MMA issued by this thread is complete before the CTA ends
+            umma::commit(bar(B_FINAL_S));
+            mbar_wait_bounded(bar(B_FINAL_S), 0u, kWaitLimit);
+        }
+        __syncwarp();
+    } else if (cnt > 0 && warp == 6) {
+        // --------------------------------------------------------- P.V MMAs
+        if (lane == 0) {
+            const uint64_t vdesc0 = umma::smem_desc_sw128(sb + kVOff, kRingRegion, 1024);
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                ok = wait_bar(bar(B_INFO + (k & 3)), (uint32_t)((k >> 2) & 1), misc);
+                if (!ok) break;
+                const ChunkInfo c = info[k & 3];
+                mbar_arrive(bar(B_INFOFREE + (k & 3)));
+                const int b = k & 1;
+                ok = wait_bar(bar(B_PFULL + b), (uint32_t)((k >> 1) & 1), misc);
+                if (!ok) break;
                 const bool start = c.b.z & 1;
-                if (start && c.b.w > 0 && !wait_bar(bar(B_OFREE), (uint32_t)((c.b.w - 1) & 1), misc))
-                    return false;
+                if (start && c.b.w > 0) {
+                    ok = wait_bar(bar(B_OFREE), (uint32_t)((c.b.w - 1) & 1), misc);
+                    if (!ok) break;
+                }
                 umma::fence_after_sync();
                 const int i = c.a.x, n = c.a.y;
                 for (int jj = 0; jj < n; ++jj) {
                     const int st = (i + jj) % kStages;
                     const uint64_t bd = vdesc0 + (uint64_t)((st * kBox) >> 4);
-                    umma::mma_bf16_ts(tmem + kColO, tmem + kColPhi + (uint32_t)(8 * jj), bd,
-                                      kIdescPV, !(start && jj == 0));
-                    umma::mma_bf16_ts(tmem + kColO, tmem + kColPlo + (uint32_t)(8 * jj), bd,
-                                      kIdescPV, true);
+                    const uint32_t ph = tmem + kColS + (uint32_t)(64 * b + 8 * jj);
+                    umma::mma_bf16_ts(tmem + kColO, ph, bd, kIdescPV, !(start && jj == 0));
+                    umma::mma_bf16_ts(tmem + kColO, ph + 32, bd, kIdescPV, true);
                 }
                 for (int jj = 0; jj < n; ++jj) umma::commit(bar(B_EMPTY + (i + jj) % kStages));
-                umma::commit(bar(B_PVDONE));
+                umma::commit(bar(B_PVDONE + b));
                 if (c.b.z & 2) umma::commit(bar(B_OFULL));
-                return true;
-            };
-            ChunkInfo cur;
-            int k = 0;
-            bool ok = plan(0, 0, cur) && issue_s(cur, 0);
-            while (ok) {
-                ChunkInfo nx;
-                const bool more = cur.a.x + cur.a.y < cnt;
-                if (more) ok = plan(cur.a.x + cur.a.y, k + 1, nx) && issue_s(nx, k + 1);
-                if (ok) ok = issue_pv(cur, k);
-                if (!more || !ok) break;
-                cur = nx;
-                ++k;
+                if (i + n >= cnt) break;
             }
-            // every MMA issued by this thread is complete before the CTA ends
-            umma::commit(bar(B_FINAL));
-            mbar_wait_bounded(bar(B_FINAL), 0u, kWaitLimit);
+            umma::commit(bar(B_FINAL_PV));
+            mbar_wait_bounded(bar(B_FINAL_PV), 0u, kWaitLimit);
         }
         __syncwarp();
     } else if (cnt > 0 && warp < nact) {
@@ -559,9 +584,9 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
         bool ok = __all_sync(kFull, wait_bar(bar(B_INFO), 0u, misc));
         if (ok) load_q(info[0].a.z);
         for (int k = 0; ok; ++k) {
-            ok = __all_sync(kFull, wait_bar(bar(B_INFO + (k & 1)), (uint32_t)((k >> 1) & 1), misc));
+            ok = __all_sync(kFull, wait_bar(bar(B_INFO + (k & 3)), (uint32_t)((k >> 2) & 1), misc));
             if (!ok) break;
-            const ChunkInfo c = info[k & 1];
+            const ChunkInfo c = info[k & 3];
             const int i = c.a.x, n = c.a.y, blk0 = c.a.w, L = c.b.x, vmask = c.b.y;
             const bool start = c.b.z & 1, end = c.b.z & 2;
             if (start) {
@@ -572,26 +597,23 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                 m_ref = -INFINITY;
                 l = 0.f;
             }
-            ok = __all_sync(kFull, wait_bar(bar(B_SFULL), (uint32_t)(k & 1), misc));
+            const int b = k & 1;
+            ok = __all_sync(kFull, wait_bar(bar(B_SFULL + b), (uint32_t)((k >> 1) & 1), misc));
             if (!ok) break;
             umma::fence_after_sync();
             uint32_t sr[kKeys];
-#pragma unroll
-            for (int h32 = 0; h32 < kKeys / 32; ++h32)
-                umma::tmem_ld32(trow + kColS + (uint32_t)(32 * h32),
-                                *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * h32]));
+            umma::tmem_ld32(trow + kColS + (uint32_t)(64 * b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            umma::tmem_ld32(trow + kColS + (uint32_t)(64 * b + 32),
+                            *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             umma::tmem_wait_ld();
-            umma::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SFREE));
             const bool more = i + n < cnt;
             // Q is no longer read once this chunk's scores exist: load the
             // next segment's rows now
             if (end && more) {
-                ok = __all_sync(kFull, wait_bar(bar(B_INFO + ((k + 1) & 1)),
-                                                (uint32_t)(((k + 1) >> 1) & 1), misc));
+                ok = __all_sync(kFull, wait_bar(bar(B_INFO + ((k + 1) & 3)),
+                                                (uint32_t)(((k + 1) >> 2) & 1), misc));
                 if (!ok) break;
-                load_q(info[(k + 1) & 1].a.z);
+                load_q(info[(k + 1) & 3].a.z);
             }
             // raw scores; keys past the context, in blocks that were not
             // fetched, of columns past the chunk and of rows past the group
@@ -638,14 +660,14 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                 m_ref = mx;
                 resc = true;
             }
-            // P and the accumulator are free once the previous chunk's P.V
-            // products are done
-            if (k >= 1) {
-                ok = __all_sync(kFull, wait_bar(bar(B_PVDONE), (uint32_t)((k - 1) & 1), misc));
+            // P goes over S in buffer b (the S issuer reuses the buffer only
+            // after the P.V products of this chunk); a rescale of the
+            // accumulator needs those of chunk k - 1
+            if (__any_sync(kFull, resc)) {
+                ok = __all_sync(kFull, wait_bar(bar(B_PVDONE + ((k - 1) & 1)),
+                                                (uint32_t)(((k - 1) >> 1) & 1), misc));
                 if (!ok) break;
                 umma::fence_after_sync();
-            }
-            if (__any_sync(kFull, resc)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -663,7 +685,7 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int half = 0; half < kKeys / 32; ++half) {
-                uint32_t hi[16], lo[16];
+                uint32_t hi[16], lo[16];       // keys 32 half .. 32 half + 31
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int cc = 32 * half + 2 * e;
@@ -677,14 +699,14 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                     hi[e] = pack_bf16x2(p0, p1);
                     lo[e] = pack_bf16x2(p0 - bf16_lo(hi[e]), p1 - bf16_hi(hi[e]));
                 }
-                umma::tmem_st16(trow + kColPhi + (uint32_t)(16 * half), hi);
-                umma::tmem_st16(trow + kColPlo + (uint32_t)(16 * half), lo);
+                umma::tmem_st16(trow + kColS + (uint32_t)(64 * b + 16 * half), hi);
+                umma::tmem_st16(trow + kColS + (uint32_t)(64 * b + 32 + 16 * half), lo);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             umma::tmem_wait_st();
             umma::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL));
+            if (lane == 0) mbar_arrive(bar(B_PFULL + b));
             if (end) {
                 // the segment's accumulator: output or partial
                 ok = __all_sync(kFull, wait_bar(bar(B_OFULL), (uint32_t)(c.b.w & 1), misc));
