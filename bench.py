@@ -41,10 +41,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "6f8b70001de92aab6e2bd34fbce919d6ab769d95aeb283588146fdc518d1b949",
-           "bytes_per_launch": 1087719424,
+TRAFFIC = {"kernel_sha256": "0110c714099be11f1267bc314aa080e9867e73c0e2d24f2787d3333403eef80c",
+           "bytes_per_launch": 1088191488,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,149,440 B + 2,780,416 B), scaled x4 by units processed "
+                     "(269,149,184 B + 2,898,688 B), scaled x4 by units processed "
                      "(profiles/smem_bank_conflicts_split_b8.md)"}
 
 
@@ -438,6 +438,9 @@ def per_config(pk, cfgs, device, stream, K, W, world, peak, read_gbs):
         gbs = kvb / (ms * 1e-3) / 1e9
         split_gbs = kvb / (m["split_ms"] * 1e-3) / 1e9
         r = {"config": workload_config(cfg), "us_per_step": ms * 1e3,
+             "kernel": ("paged_decode_wide_kernel (tcgen05)" if case.D == 128 and case.kv_dtype ==
+                        workloads.BF16 and case.Hq // case.Hkv >= 64 else
+                        "paged_decode_split_kernel (mma.sync)"),
              "kv_bytes_per_step": kvb, "kv_gbs": gbs,
              "frac_of_copy_peak": gbs / peak, "frac_of_read_ceiling": gbs / read_gbs,
              "split_us": m["split_ms"] * 1e3, "merge_us": m["merge_ms"] * 1e3,
@@ -778,7 +781,7 @@ def run_ours(args):
             "default_step_us": default_step_us,
             "unfused": unfused, "graph_replay": graph_replay}
     if not args.no_per_config and not args.batch:
-        others = [c for c in ("1", "2", "3", "4", "5a", "5b") if c != cfg]
+        others = [c for c in ("1", "2", "3", "4", "5a", "5b", "mqa64", "mqa128") if c != cfg]
         line["per_config"] = per_config(pk, others, device, stream, K, W, world, peak,
                                         rc["gbs"])
     if prefix is not None:

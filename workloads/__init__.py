@@ -48,6 +48,15 @@ CONFIGS = {
                B=32, Hq=32, Hkv=8, D=128, N=8192, kv_dtype=FP8_E4M3, slack=0.10),
     "5b": dict(desc="MHA 32q/32kv heads, d128, batch 8, 4096 prefilled + 1, bf16",
                B=8, Hq=32, Hkv=32, D=128, N=4096, kv_dtype=BF16, slack=0.10),
+    # not among the pages' five workloads: MQA ("KV cache complete guide",
+    # section "(2) GQA": one KV head shared by every query head) on a 64- or
+    # 128-head model, config 2's batch and context
+    "mqa64": dict(desc="MQA: 64 query heads on 1 KV head, d128, batch 32, 8192 prefilled + 1, "
+                       "bf16",
+                  B=32, Hq=64, Hkv=1, D=128, N=8192, kv_dtype=BF16, slack=0.10),
+    "mqa128": dict(desc="MQA: 128 query heads on 1 KV head, d128, batch 32, 8192 prefilled + 1, "
+                        "bf16",
+                   B=32, Hq=128, Hkv=1, D=128, N=8192, kv_dtype=BF16, slack=0.10),
     # not one of the pages' workloads: config 3's structure with a long shared
     # system prompt, where the shared blocks are most of the bytes
     "3L": dict(desc="shared-prompt batch: 256 seqs, 32q/8kv, d128, groups of 8 sharing a "
@@ -57,7 +66,8 @@ CONFIGS = {
 }
 
 SEED_BASE = 1000
-SEED_OFFSET = {"1": 1, "2": 2, "3": 3, "4": 4, "5a": 5, "5b": 6, "3L": 7}
+SEED_OFFSET = {"1": 1, "2": 2, "3": 3, "4": 4, "5a": 5, "5b": 6, "3L": 7, "mqa64": 8,
+               "mqa128": 9}
 
 
 @dataclass
