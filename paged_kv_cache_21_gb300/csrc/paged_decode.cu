@@ -76,7 +76,9 @@ namespace pkv {
 
 __device__ DevErr g_decode_err;
 
-constexpr int kWarps = 4;                        // warps per CTA (independent pipelines)
+// Warps per CTA (independent pipelines) per KV element type.
+constexpr int kWarpsBf16 = 4;
+constexpr int kWarpsFp8 = 4;
 // Shared memory given to each warp's ring of stages, and the CTAs per SM the
 // register allocation must allow, per KV element type.
 constexpr int kWarpStageBytesBf16 = 24576;
@@ -102,6 +104,7 @@ struct Geom {
     static constexpr int STAGE = 2 * TILE;                    // K + V
     static constexpr int STAGES_RAW = (FP8 ? kWarpStageBytesFp8 : kWarpStageBytesBf16) / STAGE;
     static constexpr int MIN_CTAS = FP8 ? kMinCtasFp8 : kMinCtasBf16;
+    static constexpr int WARPS = FP8 ? kWarpsFp8 : kWarpsBf16;
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
     static constexpr int SWZ = BOXW == 128 ? 7 : 3;           // 128B or 64B swizzle
     static constexpr int KSTEPS = D / 16;
@@ -109,11 +112,11 @@ struct Geom {
     static constexpr int CHUNKS_PER_BOXROW = BOXW / 16;
     // shared memory: [stages of every warp][mbarriers][stage metadata (int4)],
     // the stage area aligned to 1024 bytes for the swizzled bulk copies
-    static constexpr int BAR_OFF = kWarps * STAGES * STAGE;
+    static constexpr int BAR_OFF = WARPS * STAGES * STAGE;
     // one more barrier per warp that nothing arrives on (the time-out test hook)
-    static constexpr int STALL_OFF = BAR_OFF + kWarps * STAGES * 8;
-    static constexpr int META_OFF = (STALL_OFF + kWarps * 8 + 15) / 16 * 16;
-    static constexpr int SMEM = META_OFF + kWarps * STAGES * 16 + 1024;
+    static constexpr int STALL_OFF = BAR_OFF + WARPS * STAGES * 8;
+    static constexpr int META_OFF = (STALL_OFF + WARPS * 8 + 15) / 16 * 16;
+    static constexpr int SMEM = META_OFF + WARPS * STAGES * 16 + 1024;
     static_assert(TILE % 1024 == 0 && BOXB % 512 == 0, "swizzled tiles need aligned stages");
     static_assert(BAR_OFF % 8 == 0 && STALL_OFF % 8 == 0 && META_OFF % 16 == 0,
                   "barrier / metadata alignment");
@@ -884,7 +887,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
     constexpr int ST = G::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int w = blockIdx.x * kWarps + warp;
+    const int w = blockIdx.x * G::WARPS + warp;
     // Groups cut into 2^hshift sub-groups: the warps form one team per
     // sub-group, and every team partitions the same (sequence, KV head,
     // block) units the same way, so the warps of all teams that read a tile
@@ -1211,7 +1214,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tm_k, const CUtens
 
 // Plain decoding: one row tile per unit.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, Geom<D, FP8>::MIN_CTAS)
+__global__ void __launch_bounds__(Geom<D, FP8>::WARPS * 32, Geom<D, FP8>::MIN_CTAS)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
 {
@@ -1221,7 +1224,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 // Shared-prefix decoding: prefix chunks with up to 16 query rows, then the
 // sequences.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, Geom<D, FP8>::MIN_CTAS)
+__global__ void __launch_bounds__(Geom<D, FP8>::WARPS * 32, Geom<D, FP8>::MIN_CTAS)
 paged_decode_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const DecodeParams p)
 {
@@ -1436,7 +1439,7 @@ int variant_setup(VariantInfo& vi)
         cudaSuccess)
         return KV_ERR_CUDA;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kWarps * 32, G::SMEM) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, G::WARPS * 32, G::SMEM) !=
             cudaSuccess ||
         n <= 0)
         return KV_ERR_CUDA;
@@ -1449,6 +1452,12 @@ template <int D, bool FP8>
 int variant_setup_nr(VariantInfo& vi, int nr)
 {
     return nr == 2 ? variant_setup<D, FP8, 2>(vi) : variant_setup<D, FP8, 1>(vi);
+}
+
+int warps_per_cta(int D, bool fp8)
+{
+    if (D == 128) return fp8 ? Geom<128, true>::WARPS : Geom<128, false>::WARPS;
+    return fp8 ? Geom<64, true>::WARPS : Geom<64, false>::WARPS;
 }
 
 // Device facts and per-variant occupancy, cached per device.
@@ -1656,7 +1665,7 @@ int plan_launch(int B, int nc, int Hq, int Hkv, int D, bool fp8, LaunchPlan& lp)
     }
     if (int rc = device_info(D, fp8, lp.nr, sms, cps)) return rc;
     lp.grid = sms * cps;
-    lp.warps_total = lp.grid * kWarps;
+    lp.warps_total = lp.grid * warps_per_cta(D, fp8);
     lp.slot_warps = nc > 0 ? 2 * lp.warps_total : lp.warps_total;
     lp.ws = ws_layout(B, nc, Hq, lp.hs.Hkv_v, D, lp.slot_warps, lp.nr);
     return KV_OK;
@@ -1702,9 +1711,9 @@ cudaError_t launch_split(int nr, unsigned grid, cudaStream_t st, const CUtensorM
                          const CUtensorMap& mv, const DecodeParams& dp)
 {
     if (nr == 2)
-        return launch_pdl(paged_decode_prefix_kernel<D, FP8>, grid, kWarps * 32,
+        return launch_pdl(paged_decode_prefix_kernel<D, FP8>, grid, Geom<D, FP8>::WARPS * 32,
                           Geom<D, FP8>::SMEM, st, mk, mv, dp);
-    return launch_pdl(paged_decode_split_kernel<D, FP8>, grid, kWarps * 32, Geom<D, FP8>::SMEM,
+    return launch_pdl(paged_decode_split_kernel<D, FP8>, grid, Geom<D, FP8>::WARPS * 32, Geom<D, FP8>::SMEM,
                       st, mk, mv, dp);
 }
 
@@ -2010,7 +2019,7 @@ extern "C" int kv_prefix_plan(const int32_t* block_tables, int max_blocks_per_se
         // the plain split kernel's persistent grid on the current device
         int sms = 0, cps = 0;
         if (int rc = device_info(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3, 1, sms, cps)) return rc;
-        resident_warps = sms * cps * kWarps;
+        resident_warps = sms * cps * warps_per_cta(head_dim, kv_dtype == KV_DTYPE_FP8_E4M3);
     }
     return prefix_plan_host(block_tables, max_blocks_per_seq, context_lens, num_seqs,
                             num_q_heads / num_kv_heads, num_kv_heads, resident_warps, chunks,
