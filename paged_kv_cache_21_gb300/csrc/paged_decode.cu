@@ -1838,6 +1838,7 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
         wp.sl2 = dp.sl2;
         wp.out_f32 = dp.out_f32;
         wp.early = dp.early;
+        wp.test_stall = dp.test_stall;
         err = wide_launch(mk, mv, wp, st);
     } else if (head_dim == 128) {
         err = fp8 ? launch_split<128, true>(nr, grid, st, mk, mv, dp)

@@ -89,6 +89,7 @@ enum Bar {
     B_OFREE,                     // the row threads have read it
     B_FINAL_S,                   // every score MMA of the CTA is done
     B_FINAL_PV,                  // every P.V MMA of the CTA is done
+    B_STALL,                     // nothing arrives here (the time-out test hook)
     kNumBars
 };
 constexpr int kMetaOff = kBarOff + (kNumBars * 8 + 15) / 16 * 16;
@@ -262,6 +263,7 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
         mbar_init(bar(B_OFREE), nact);
         mbar_init(bar(B_FINAL_S), 1);
         mbar_init(bar(B_FINAL_PV), 1);
+        mbar_init(bar(B_STALL), 1);
         misc[M_ABORT] = 0;
         fence_mbar_init();
     }
@@ -442,6 +444,13 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
             bool prev_end = true;
             // wait for a chunk's tiles (and edits), describe it to the row threads
             auto plan = [&](int i, int k, ChunkInfo& c) -> bool {
+                // test hook: the first wait of the CTA on a barrier that nothing
+                // arrives on, for test_stall clocks; every role then stops
+                if (k == 0 && p.test_stall > 0 && !mbar_wait_bounded(bar(B_STALL), 0u, p.test_stall)) {
+                    misc[M_ABORT] = 1;
+                    raise_flag(&g_wide_err, KV_DEVERR_PIPELINE_TIMEOUT, blockIdx.x);
+                    return false;
+                }
                 // entry k & 3 last described chunk k - 4: the P.V warp must be done with it
                 if (k >= 4 && !wait_bar(bar(B_INFOFREE + (k & 3)), (uint32_t)(((k - 4) >> 2) & 1), misc))
                     return false;

@@ -32,6 +32,7 @@ struct WideParams {
     float sl2;                 // scale * log2(e)
     int out_f32;
     int early;                 // read tables and caches before the dependency wait
+    long long test_stall;      // > 0: test hook, see kv_test_pipeline_stall
 };
 
 // Shared memory of the kernel and the CTAs one SM holds (cached per device).

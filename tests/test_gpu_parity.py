@@ -601,7 +601,7 @@ def test_bad_inputs_are_flagged_not_faulted():
     assert float(x.sum()) == 8.0
 
 
-@pytest.mark.parametrize("prefix", [False, True], ids=["plain", "prefix_chunks"])
+@pytest.mark.parametrize("prefix", [False, True, "wide"], ids=["plain", "prefix_chunks", "wide"])
 @pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
 def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, prefix):
     """The bounded wait on a bulk copy: with the test hook every warp's first
@@ -613,7 +613,12 @@ def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, pref
     case = workloads.make_custom(6, 32, 8, 128, [1, 17, 300, 4097, 2000, 33],
                                  kv_dtype=kv_dtype, seed=93)
     pre = None
-    if prefix:
+    if prefix == "wide":
+        # 128 query rows on one KV head: the tensor-memory kernel (bf16 only;
+        # the E4M3 case runs the sub-group kernel)
+        case = workloads.make_custom(6, 128, 1, 128, [1, 17, 300, 4097, 2000, 33],
+                                     kv_dtype=kv_dtype, seed=95)
+    elif prefix:
         case = workloads.make_case("3", override={"B": 16, "N_hi": 3000, "kv_dtype": kv_dtype},
                                    seed=94)
         pre = pk.prefix_chunks(case.block_tables, case.context_lens, case.G)
@@ -625,7 +630,9 @@ def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, pref
     finally:
         pk.set_pipeline_stall(0)
     flags, detail = pk.get_device_error()
-    assert flags == pk.DEVERR_PIPELINE_TIMEOUT and detail == 0, (flags, detail)
+    assert flags == pk.DEVERR_PIPELINE_TIMEOUT, (flags, detail)
+    if prefix != "wide" or kv_dtype != workloads.BF16:
+        assert detail == 0, detail               # the split kernel reports the unit
     x = torch.ones(4, device="cuda") * 2
     assert float(x.sum()) == 8.0
     out, kc, vc = H.gpu_step(case, fused=True, early_inputs=True, prefix=pre)
@@ -690,11 +697,13 @@ def test_workspace_needs_no_initialisation():
         assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-def test_fused_step_replays_in_a_cuda_graph():
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (128, 1)])
+def test_fused_step_replays_in_a_cuda_graph(Hq, Hkv):
     """A captured fused step keeps one counter epoch for every replay; each
-    replay must still merge correctly (the append rewrites the same token)."""
+    replay must still merge correctly (the append rewrites the same token).
+    128 rows on one KV head: the tensor-memory kernel in a graph."""
     import paged_kv_cache_21_gb300 as pk
-    case = workloads.make_custom(4, 32, 8, 128, [5000, 70, 12000, 4097], seed=45)
+    case = workloads.make_custom(4, Hq, Hkv, 128, [5000, 70, 12000, 4097], seed=45)
     out_ref, kc, vc = H.gpu_step(case, fused=True)          # first call: per-device set-up
     q = case.q.cuda()
     kn, vn = case.k_new.cuda(), case.v_new.cuda()
@@ -855,8 +864,9 @@ def test_token_by_token_decode_equals_causal_prefill(kv_dtype):
         assert err < tol, (t, err)
 
 
-@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
-def test_back_to_back_decode_loop_with_early_inputs(kv_dtype):
+@pytest.mark.parametrize("kv_dtype,Hq,Hkv", [(workloads.BF16, 8, 2), (workloads.FP8_E4M3, 8, 2),
+                                             (workloads.BF16, 128, 1)])
+def test_back_to_back_decode_loop_with_early_inputs(kv_dtype, Hq, Hkv):
     """The token-by-token decode of two sequences as one stream of launches
     with no host synchronisation between steps: every step's tables are
     uploaded before the loop, then paged_decode runs step after step with
@@ -866,7 +876,7 @@ def test_back_to_back_decode_loop_with_early_inputs(kv_dtype):
     and the outputs equal those of the same loop with the default ordering,
     bit for bit."""
     import paged_kv_cache_21_gb300 as pk
-    Hq, Hkv, D, T, NB, MB = 8, 2, 128, 90, 16, 8
+    D, T, NB, MB = 128, 90, 16, 8
     g = torch.Generator().manual_seed(191 + kv_dtype)
     Q = torch.randn((2, T, Hq, D), generator=g).to(torch.bfloat16)
     Kt = torch.randn((2, T, Hkv, D), generator=g).to(torch.bfloat16)
