@@ -105,6 +105,22 @@ def test_gpu_entry_points_reject_bad_arguments_without_a_gpu(lib_path):
                                     0, 32, 8, 128, 0.1, None, 0, None) == pk.KV_OK
 
 
+def test_measurement_hooks_reject_bad_arguments_without_a_gpu(lib_path):
+    import paged_kv_cache_21_gb300 as pk
+    L = pk._lib
+    sink = ctypes.c_void_p(64)
+    # kv_read_ceiling: no buffer, no bytes, a size or an address off 16 bytes
+    assert L.kv_read_ceiling(None, 4096, sink, None) == pk.KV_ERR_INVALID_ARG
+    assert L.kv_read_ceiling(ctypes.c_void_p(4096), 0, sink, None) == pk.KV_ERR_INVALID_ARG
+    assert L.kv_read_ceiling(ctypes.c_void_p(4096), 4100, sink, None) == pk.KV_ERR_INVALID_ARG
+    assert L.kv_read_ceiling(ctypes.c_void_p(4104), 4096, sink, None) == pk.KV_ERR_INVALID_ARG
+    assert L.kv_read_ceiling(ctypes.c_void_p(4096), 4096, None, None) == pk.KV_ERR_INVALID_ARG
+    # paged_decode_timed shares paged_decode's shape checks (head_dim 96)
+    assert L.paged_decode_timed(None, 0, None, None, None, None, None, 0, 1.0, 1.0, 1, None, 1,
+                                None, 1, 32, 8, 96, 0.1, None, None, 0, 0, None, 0, None, None,
+                                None, None) == pk.KV_ERR_UNSUPPORTED
+
+
 def test_fast_call_module_marshals_only(lib_path):
     """The CPython-API module, when built, exposes the four per-step calls
     and checks only the argument list (a wrong one fails before any call)."""

@@ -699,9 +699,10 @@ def test_workspace_needs_no_initialisation():
 
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (128, 1)])
 def test_fused_step_replays_in_a_cuda_graph(Hq, Hkv):
-    """A captured fused step keeps one counter epoch for every replay; each
-    replay must still merge correctly (the append rewrites the same token).
-    128 rows on one KV head: the tensor-memory kernel in a graph."""
+    """A captured fused step replays with the same arguments: each replay
+    appends the same token again and must give the same output (the merge
+    reads only what that replay's split kernel wrote).  128 rows on one KV
+    head: the tensor-memory kernel in a graph."""
     import paged_kv_cache_21_gb300 as pk
     case = workloads.make_custom(4, Hq, Hkv, 128, [5000, 70, 12000, 4097], seed=45)
     out_ref, kc, vc = H.gpu_step(case, fused=True)          # first call: per-device set-up
@@ -986,3 +987,53 @@ def test_fast_calls_match_ctypes_calls_and_share_the_library():
     pk.paged_decode(out_c, q, kc, vc, bad, cl, case.scale, ws)
     torch.cuda.synchronize()
     assert pk.get_device_error() == (pk.DEVERR_BLOCK_OUT_OF_RANGE, case.num_blocks + 7)
+
+
+def test_read_ceiling_reads_every_piece():
+    """The read-only ceiling hook reads every 8 KB piece of its buffer (the
+    last one partial here): its XOR sink equals the XOR of the first word of
+    every piece, computed on the host, and no copy timed out."""
+    import paged_kv_cache_21_gb300 as pk
+    nbytes = 8192 * 3001 + 4096 + 16
+    g = torch.Generator(device="cuda").manual_seed(11)
+    buf = torch.randint(-2**31, 2**31 - 1, (nbytes // 4,), dtype=torch.int32, device="cuda",
+                        generator=g)
+    sink = torch.zeros(2, dtype=torch.int32, device="cuda")
+    pk.read_ceiling(buf, sink)
+    torch.cuda.synchronize()
+    words = buf.cpu().numpy().view(np.uint32)
+    want = np.bitwise_xor.reduce(words[:: 8192 // 4])
+    got = sink.cpu().numpy().view(np.uint32)
+    assert got[1] == 0
+    assert got[0] == want
+
+
+@pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
+def test_timed_call_matches_the_plain_call(kv_dtype):
+    """paged_decode_timed runs the same kernels as paged_decode and only adds
+    event records: the outputs are bit-identical and the three events are in
+    order."""
+    import paged_kv_cache_21_gb300 as pk
+    case = workloads.make_custom(6, 32, 8, 128, [9000, 17, 4097, 2500, 1, 700], seed=46,
+                                 kv_dtype=kv_dtype)
+    out_ref, kc, vc = H.gpu_step(case, fused=True)
+    q, kn, vn = case.q.cuda(), case.k_new.cuda(), case.v_new.cuda()
+    bt = torch.from_numpy(case.block_tables).cuda()
+    cl = torch.from_numpy(case.context_lens).cuda()
+    ws = pk.alloc_workspace(case.B, case.Hq, case.Hkv, case.D)
+    out_a = torch.empty_like(out_ref)
+    out_b = torch.empty_like(out_ref)
+    # the caches already hold the step's token: both calls rewrite the same bytes
+    pk.paged_decode(out_a, q, kc, vc, bt, cl, case.scale, ws, case.k_scale, case.v_scale,
+                    k_new=kn, v_new=vn)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in ev:
+        e.record()
+    pk.paged_decode_timed(out_b, q, kc, vc, bt, cl, case.scale, ws, ev, case.k_scale,
+                          case.v_scale, k_new=kn, v_new=vn)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(out_a.view(torch.int16), out_ref.view(torch.int16))
+    split = ev[0].elapsed_time(ev[1])
+    total = ev[0].elapsed_time(ev[2])
+    assert 0.0 < split <= total
