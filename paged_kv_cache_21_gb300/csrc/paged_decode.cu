@@ -1656,7 +1656,7 @@ int plan_launch(int B, int nc, int Hq, int Hkv, int D, bool fp8, LaunchPlan& lp)
         // partial slots of one sub-group: one per (sequence, KV head) plus
         // one per CTA (a CTA's partial of pair x goes to slot x + CTA)
         sms = num_sms_current();
-        if (int rc = wide_setup(cps)) return rc;
+        if (int rc = wide_setup(Hq / Hkv, cps)) return rc;
         lp.grid = sms * cps;
         lp.warps_total = lp.grid;
         lp.slot_warps = lp.grid << lp.hs.hshift;

@@ -20,7 +20,8 @@
 // How:
 //  * Persistent grid, two CTAs per SM; each CTA takes an equal contiguous
 //    range of the flat (sequence, KV head, block) units.  Warp 4 streams the
-//    K and V tiles of its units into a 9-stage ring with TMA (the split
+//    K and V tiles of its units into a ring of 9 stages (11 when the group has
+//    at most 64 rows and Q needs half the buffer) with TMA (the split
 //    kernel's tensor maps, 128-byte swizzle; the K tiles of consecutive
 //    stages form one contiguous operand) and does the fused append; warp 5
 //    allocates tensor memory and issues the score MMAs, warp 6 the P.V MMAs;
@@ -64,38 +65,7 @@ constexpr int D = 128;
 constexpr int kRows = 128;                      // M of every MMA
 constexpr int kChunk = 4;                       // blocks per chunk
 constexpr int kKeys = kChunk * kBlock;          // keys per chunk (S columns)
-constexpr int kStages = 9;                      // ring stages (one block's K and V)
 constexpr int kBox = kBlock * 128;              // one box: 16 rows x 128 bytes
-constexpr int kRegion = kRows * 128;            // 128 rows x 128 bytes
-constexpr int kRingRegion = kStages * kBox;     // one box of every stage, contiguous
-constexpr int kQOff = 0;                        // Q: 2 regions (d 0-63, 64-127)
-constexpr int kKOff = kQOff + 2 * kRegion;      // K: box 0 of all stages, then box 1
-constexpr int kVOff = kKOff + 2 * kRingRegion;  // V: likewise
-constexpr int kBarOff = kVOff + 2 * kRingRegion;
-enum Bar {
-    B_FULL = 0,                  // + stage: the tiles have landed
-    B_EMPTY = kStages,           // + stage: the MMAs reading them are done
-    B_PATCH = 2 * kStages,       // + stage: the copy warp has edited the tiles
-    B_QFULL = 3 * kStages,       // Q of the next segment is in place
-    B_INFO,                      // + entry (4): the chunk description is written
-    B_INFOFREE = B_INFO + 4,     // + entry (4): the P.V warp has read it
-    B_SFULL = B_INFOFREE + 4,    // + buffer: S computed
-    B_SFULL1,
-    B_PFULL,                     // + buffer: P written
-    B_PFULL1,
-    B_PVDONE,                    // + buffer: the P.V MMAs reading that P are done
-    B_PVDONE1,
-    B_OFULL,                     // the segment's accumulator is complete
-    B_OFREE,                     // the row threads have read it
-    B_FINAL_S,                   // every score MMA of the CTA is done
-    B_FINAL_PV,                  // every P.V MMA of the CTA is done
-    B_STALL,                     // nothing arrives here (the time-out test hook)
-    kNumBars
-};
-constexpr int kMetaOff = kBarOff + (kNumBars * 8 + 15) / 16 * 16;
-constexpr int kInfoOff = kMetaOff + kStages * 16;     // 4 entries x 2 int4
-constexpr int kMiscOff = kInfoOff + 4 * 32;
-constexpr int kSmem = kMiscOff + 64 + 1024;
 constexpr uint32_t kTmemCols = 256;
 // tensor memory: buffer b at columns 64b holds S of a chunk (64 keys, f32),
 // then, in place, its P (32 columns of bf16 pairs for the high parts, then 32
@@ -105,9 +75,44 @@ constexpr uint32_t kColO = 128;
 constexpr int kThreads = 224;                   // 7 warps
 constexpr long long kWaitLimit = 1LL << 31;    // ~1 s of SM clocks
 constexpr uint32_t kIdescPV = umma::idesc_bf16_f32(kRows, D, false, true);
-static_assert(kSmem <= 232448 / 2 - 1024, "two CTAs per SM");
-static_assert(kRegion % 1024 == 0 && kRingRegion % 1024 == 0 && kKOff % 1024 == 0,
-              "swizzled operands need 1024-byte aligned atoms");
+
+// Shared-memory layout for a Q buffer of QR rows (the group's rows, 64 or
+// 128; the 128-row MMAs read rows past QR from the memory that follows, and
+// the rows of S they give are never read) and the ring that fills the rest of
+// half an SM: the Q rows a group of up to 64 rows leaves free buy two stages.
+template <int QR>
+struct Layout {
+    static constexpr int kRegion = QR * 128;           // QR rows x 128 bytes
+    static constexpr int kStages = QR <= 64 ? 11 : 9;  // ring stages (one block's K and V)
+    static constexpr int kRingRegion = kStages * kBox; // one box of every stage, contiguous
+    static constexpr int kQOff = 0;                    // Q: 2 regions (d 0-63, 64-127)
+    static constexpr int kKOff = kQOff + 2 * kRegion;  // K: box 0 of all stages, then box 1
+    static constexpr int kVOff = kKOff + 2 * kRingRegion;  // V: likewise
+    static constexpr int kBarOff = kVOff + 2 * kRingRegion;
+    // barriers
+    static constexpr int B_FULL = 0;                   // + stage: the tiles have landed
+    static constexpr int B_EMPTY = kStages;            // + stage: the MMAs reading them are done
+    static constexpr int B_PATCH = 2 * kStages;        // + stage: the copy warp has edited the tiles
+    static constexpr int B_QFULL = 3 * kStages;        // Q of the next segment is in place
+    static constexpr int B_INFO = B_QFULL + 1;         // + entry (4): the chunk description is written
+    static constexpr int B_INFOFREE = B_INFO + 4;      // + entry (4): the P.V warp has read it
+    static constexpr int B_SFULL = B_INFOFREE + 4;     // + buffer (2): S computed
+    static constexpr int B_PFULL = B_SFULL + 2;        // + buffer (2): P written
+    static constexpr int B_PVDONE = B_PFULL + 2;       // + buffer (2): the P.V MMAs reading that P are done
+    static constexpr int B_OFULL = B_PVDONE + 2;       // the segment's accumulator is complete
+    static constexpr int B_OFREE = B_OFULL + 1;        // the row threads have read it
+    static constexpr int B_FINAL_S = B_OFREE + 1;      // every score MMA of the CTA is done
+    static constexpr int B_FINAL_PV = B_FINAL_S + 1;   // every P.V MMA of the CTA is done
+    static constexpr int B_STALL = B_FINAL_PV + 1;     // nothing arrives here (the time-out test hook)
+    static constexpr int kNumBars = B_STALL + 1;
+    static constexpr int kMetaOff = kBarOff + (kNumBars * 8 + 15) / 16 * 16;
+    static constexpr int kInfoOff = kMetaOff + kStages * 16;   // 4 entries x 2 int4
+    static constexpr int kMiscOff = kInfoOff + 4 * 32;
+    static constexpr int kSmem = kMiscOff + 64 + 1024;
+    static_assert(kSmem <= 232448 / 2 - 1024, "two CTAs per SM");
+    static_assert(kRegion % 1024 == 0 && kRingRegion % 1024 == 0 && kKOff % 1024 == 0,
+                  "swizzled operands need 1024-byte aligned atoms");
+};
 
 // misc words: [0] tensor-memory base, [1] abort, [2] range start, [3] units,
 // [4] units per CTA, [5..7] first unit's (sequence, head, block)
@@ -116,10 +121,11 @@ enum Misc { M_TMEM = 0, M_ABORT, M_B0, M_CNT, M_Q, M_S0, M_H0, M_J0 };
 // Byte offset of 16-byte chunk c (8 elements) of row r of a stage's tile
 // inside its ring (box c / 8 in the second region), as the bulk copy lays
 // it out with the 128-byte swizzle (16-byte chunk index XOR row % 8).
+template <int RING>
 __device__ __forceinline__ uint32_t ring_off(int st, int r, int c)
 {
     const uint32_t a = (uint32_t)(r * 128 + (c & 7) * 16);
-    return (uint32_t)((c >> 3) * kRingRegion + st * kBox) + (a ^ (((a >> 7) & 7u) << 4));
+    return (uint32_t)((c >> 3) * RING + st * kBox) + (a ^ (((a >> 7) & 7u) << 4));
 }
 
 // Row r, 16-byte chunk c of a [128 rows x 128 B] region (128-byte swizzle).
@@ -221,10 +227,20 @@ struct ChunkInfo {
 
 // ------------------------------------------------------------------ kernel
 
+template <int QR>
 __global__ void __launch_bounds__(kThreads, 2)
 paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const WideParams p)
 {
+    using Ly = Layout<QR>;
+    constexpr int kStages = Ly::kStages, kRegion = Ly::kRegion, kRingRegion = Ly::kRingRegion;
+    constexpr int kQOff = Ly::kQOff, kKOff = Ly::kKOff, kVOff = Ly::kVOff, kBarOff = Ly::kBarOff;
+    constexpr int kMetaOff = Ly::kMetaOff, kInfoOff = Ly::kInfoOff, kMiscOff = Ly::kMiscOff;
+    constexpr int B_FULL = Ly::B_FULL, B_EMPTY = Ly::B_EMPTY, B_PATCH = Ly::B_PATCH;
+    constexpr int B_QFULL = Ly::B_QFULL, B_INFO = Ly::B_INFO, B_INFOFREE = Ly::B_INFOFREE;
+    constexpr int B_SFULL = Ly::B_SFULL, B_PFULL = Ly::B_PFULL, B_PVDONE = Ly::B_PVDONE;
+    constexpr int B_OFULL = Ly::B_OFULL, B_OFREE = Ly::B_OFREE, B_FINAL_S = Ly::B_FINAL_S;
+    constexpr int B_FINAL_PV = Ly::B_FINAL_PV, B_STALL = Ly::B_STALL;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sraw = smem_u32(smem_raw);
     const uint32_t sb = (sraw + 1023u) & ~1023u;
@@ -401,7 +417,7 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                 if (!valid) {
                     // no copy: a zero V tile (the row threads mask every key)
                     for (int c = lane; c < kBlock * 16; c += 32)
-                        sts128(vst + ring_off(st, c >> 4, c & 15), make_uint4(0, 0, 0, 0));
+                        sts128(vst + ring_off<kRingRegion>(st, c >> 4, c & 15), make_uint4(0, 0, 0, 0));
                 } else {
                     if (append && j == nb - 1) {
                         // the step's new token: position L - 1 of its last block
@@ -413,11 +429,11 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const uint4 x = __ldg(reinterpret_cast<const uint4*>(
                             (isv ? p.v_new : p.k_new) + srco));
                         *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + dsto * 2) = x;
-                        sts128((isv ? vst : kst) + ring_off(st, r, c), x);
+                        sts128((isv ? vst : kst) + ring_off<kRingRegion>(st, r, c), x);
                     }
                     // V rows past the context may hold anything (0 * NaN is NaN)
                     for (int c = lane; c < (kBlock - nvalid) * 16; c += 32)
-                        sts128(vst + ring_off(st, nvalid + (c >> 4), c & 15),
+                        sts128(vst + ring_off<kRingRegion>(st, nvalid + (c >> 4), c & 15),
                                make_uint4(0, 0, 0, 0));
                 }
                 fence_proxy_async_smem();
@@ -792,69 +808,85 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 std::mutex g_wide_mu;
-bool g_wide_ready[64] = {};
-int g_wide_ctas[64] = {};
+bool g_wide_ready[64][2] = {};
+int g_wide_ctas[64][2] = {};
+
+// Q rows of the instantiation a group of G rows uses
+inline int qrows_for(int G) { return G <= 64 ? 64 : 128; }
+
+template <int QR>
+int wide_setup_variant(int dev, int& n_out)
+{
+    using Ly = Layout<QR>;
+    const auto fn = paged_decode_wide_kernel<QR>;
+    // two CTAs per SM need the largest shared-memory carveout
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return KV_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, Ly::kSmem) != cudaSuccess)
+        return KV_ERR_CUDA;
+    // the kernel is sized for two CTAs per SM (shared memory, registers,
+    // tensor memory: 2 x 256 of 512 columns); the occupancy query has
+    // reported one here while the hardware placed two, so the CTAs per SM
+    // are also derived from the function's registers and shared memory
+    cudaFuncAttributes fa;
+    int smem_sm = 0, smem_rsv = 0, regs_sm = 0;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) !=
+            cudaSuccess)
+        return KV_ERR_CUDA;
+    int by_smem = smem_sm / (Ly::kSmem + (int)fa.sharedSizeBytes + smem_rsv);
+    int by_regs = fa.numRegs > 0 ? regs_sm / (fa.numRegs * kThreads) : 1;
+    int own = by_smem < by_regs ? by_smem : by_regs;
+    if (own > (int)(512 / kTmemCols)) own = 512 / kTmemCols;
+    if (own > n) n = own;
+    if (n <= 0) return KV_ERR_CUDA;
+    n_out = n;
+    return KV_OK;
+}
 
 }  // namespace
 
-int wide_setup(int& ctas_per_sm)
+int wide_setup(int G, int& ctas_per_sm)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KV_ERR_CUDA;
+    const int v = qrows_for(G) == 64 ? 0 : 1;
     std::lock_guard<std::mutex> lk(g_wide_mu);
-    if (!g_wide_ready[dev]) {
-        // two CTAs per SM need the largest shared-memory carveout
-        if (cudaFuncSetAttribute(paged_decode_wide_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(paged_decode_wide_kernel,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-            return KV_ERR_CUDA;
+    if (!g_wide_ready[dev][v]) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_wide_kernel, kThreads,
-                                                          kSmem) != cudaSuccess)
-            return KV_ERR_CUDA;
-        // the kernel is sized for two CTAs per SM (shared memory, registers,
-        // tensor memory: 2 x 256 of 512 columns); the occupancy query has
-        // reported one here while the hardware placed two, so the CTAs per SM
-        // are also derived from the function's registers and shared memory
-        cudaFuncAttributes fa;
-        int smem_sm = 0, smem_rsv = 0, regs_sm = 0;
-        if (cudaFuncGetAttributes(&fa, paged_decode_wide_kernel) != cudaSuccess ||
-            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
-                cudaSuccess ||
-            cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
-                cudaSuccess ||
-            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) !=
-                cudaSuccess)
-            return KV_ERR_CUDA;
-        int by_smem = smem_sm / (kSmem + fa.sharedSizeBytes + smem_rsv);
-        int by_regs = fa.numRegs > 0 ? regs_sm / (fa.numRegs * kThreads) : 1;
-        int own = by_smem < by_regs ? by_smem : by_regs;
-        if (own > (int)(512 / kTmemCols)) own = 512 / kTmemCols;
-        if (own > n) n = own;
-        if (n <= 0) return KV_ERR_CUDA;
-        g_wide_ctas[dev] = n;
-        g_wide_ready[dev] = true;
+        if (int rc = v == 0 ? wide_setup_variant<64>(dev, n) : wide_setup_variant<128>(dev, n))
+            return rc;
+        g_wide_ctas[dev][v] = n;
+        g_wide_ready[dev][v] = true;
     }
-    ctas_per_sm = g_wide_ctas[dev];
+    ctas_per_sm = g_wide_ctas[dev][v];
     return KV_OK;
 }
 
 cudaError_t wide_launch(const CUtensorMap& mk, const CUtensorMap& mv, const WideParams& p,
                         cudaStream_t st)
 {
+    const bool q64 = qrows_for(p.G) == 64;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.nctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = q64 ? Layout<64>::kSmem : Layout<128>::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_wide_kernel, mk, mv, p);
+    return q64 ? cudaLaunchKernelEx(&cfg, paged_decode_wide_kernel<64>, mk, mv, p)
+               : cudaLaunchKernelEx(&cfg, paged_decode_wide_kernel<128>, mk, mv, p);
 }
 
 int wide_read_error(unsigned* flags, long long* detail)

@@ -35,8 +35,9 @@ struct WideParams {
     long long test_stall;      // > 0: test hook, see kv_test_pipeline_stall
 };
 
-// Shared memory of the kernel and the CTAs one SM holds (cached per device).
-int wide_setup(int& ctas_per_sm);
+// The CTAs one SM holds of the instantiation a group of G rows uses (cached
+// per device).
+int wide_setup(int G, int& ctas_per_sm);
 // Launch with programmatic stream serialisation; grid = p.nctas.
 cudaError_t wide_launch(const CUtensorMap& mk, const CUtensorMap& mv, const WideParams& p,
                         cudaStream_t st);
