@@ -270,22 +270,24 @@ def test_mqa_full_size_and_deterministic(Hq):
     assert pk.get_device_error()[0] == 0
 
 
+@pytest.mark.parametrize("Hq", [64, 128])
 @pytest.mark.parametrize("lens", [[100000], [30000, 1, 17, 20000]])
-def test_wide_groups_split_over_many_ctas(lens):
-    """128 query rows on one KV head with pairs cut across tens of CTAs of
-    the tensor-memory kernel (partials in sub-groups of 16 rows, then the
+def test_wide_groups_split_over_many_ctas(lens, Hq):
+    """64 or 128 query rows on one KV head with pairs cut across tens of CTAs
+    of the tensor-memory kernel (partials in sub-groups of 16 rows, then the
     merge), short pairs seen whole by one CTA beside them."""
-    case = workloads.make_custom(len(lens), 128, 1, 128, lens, seed=len(lens) + 77)
+    case = workloads.make_custom(len(lens), Hq, 1, 128, lens, seed=len(lens) + 77)
     check_case(case, what="wide %s" % lens, fused=True, early_inputs=True)
     check_case(case, what="wide f32 %s" % lens, out_dtype=torch.float32)
 
 
-def test_wide_groups_flag_bad_block_ids():
+@pytest.mark.parametrize("Hq", [64, 128])
+def test_wide_groups_flag_bad_block_ids(Hq):
     """A block id outside the pool in the tensor-memory kernel is not
     fetched: its keys are masked, KV_DEVERR_BLOCK_OUT_OF_RANGE is raised with
     the id, nothing faults and the rest of the batch is unaffected."""
     import paged_kv_cache_21_gb300 as pk
-    case = workloads.make_custom(3, 128, 1, 128, [40, 300, 700], seed=91)
+    case = workloads.make_custom(3, Hq, 1, 128, [40, 300, 700], seed=91)
     out_ok, kc, vc = H.gpu_step(case, out_dtype=torch.float32)
     pk.get_device_error()
     bt = torch.from_numpy(case.block_tables).cuda()
@@ -346,7 +348,7 @@ def test_empty_contexts_give_zeros(Hq, Hkv):
     assert err < 2e-3
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (48, 1), (128, 1)])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (48, 1), (64, 1), (128, 1)])
 def test_nan_canaries_in_unused_slots_are_never_read(Hq, Hkv):
     case = workloads.make_custom(4, Hq, Hkv, 128, [1, 18, 333, 1000], seed=8, slack=0.5)
     used = np.zeros(case.num_blocks * 16, dtype=bool)
@@ -601,7 +603,8 @@ def test_bad_inputs_are_flagged_not_faulted():
     assert float(x.sum()) == 8.0
 
 
-@pytest.mark.parametrize("prefix", [False, True, "wide"], ids=["plain", "prefix_chunks", "wide"])
+@pytest.mark.parametrize("prefix", [False, True, "wide", "wide64"],
+                         ids=["plain", "prefix_chunks", "wide", "wide64"])
 @pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
 def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, prefix):
     """The bounded wait on a bulk copy: with the test hook every warp's first
@@ -613,11 +616,12 @@ def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, pref
     case = workloads.make_custom(6, 32, 8, 128, [1, 17, 300, 4097, 2000, 33],
                                  kv_dtype=kv_dtype, seed=93)
     pre = None
-    if prefix == "wide":
-        # 128 query rows on one KV head: the tensor-memory kernel (bf16 only;
-        # the E4M3 case runs the sub-group kernel)
-        case = workloads.make_custom(6, 128, 1, 128, [1, 17, 300, 4097, 2000, 33],
-                                     kv_dtype=kv_dtype, seed=95)
+    if prefix in ("wide", "wide64"):
+        # 128 (or 64) query rows on one KV head: the tensor-memory kernel with
+        # the 128-row (64-row) Q buffer (bf16 only; the E4M3 case runs the
+        # sub-group kernel)
+        case = workloads.make_custom(6, 128 if prefix == "wide" else 64, 1, 128,
+                                     [1, 17, 300, 4097, 2000, 33], kv_dtype=kv_dtype, seed=95)
     elif prefix:
         case = workloads.make_case("3", override={"B": 16, "N_hi": 3000, "kv_dtype": kv_dtype},
                                    seed=94)
@@ -631,7 +635,7 @@ def test_pipeline_timeout_is_flagged_and_the_context_stays_usable(kv_dtype, pref
         pk.set_pipeline_stall(0)
     flags, detail = pk.get_device_error()
     assert flags == pk.DEVERR_PIPELINE_TIMEOUT, (flags, detail)
-    if prefix != "wide" or kv_dtype != workloads.BF16:
+    if prefix not in ("wide", "wide64") or kv_dtype != workloads.BF16:
         assert detail == 0, detail               # the split kernel reports the unit
     x = torch.ones(4, device="cuda") * 2
     assert float(x.sum()) == 8.0
@@ -697,7 +701,7 @@ def test_workspace_needs_no_initialisation():
         assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (128, 1)])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (64, 1), (128, 1)])
 def test_fused_step_replays_in_a_cuda_graph(Hq, Hkv):
     """A captured fused step replays with the same arguments: each replay
     appends the same token again and must give the same output (the merge
