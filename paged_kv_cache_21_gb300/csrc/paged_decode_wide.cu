@@ -33,10 +33,10 @@
 //    applies the length mask, keeps a reference maximum that moves only when
 //    the chunk maximum exceeds it by more than 2^8 (then the accumulator row
 //    is rescaled in tensor memory), and stores P = 2^(x - m) split into bf16
-//    high and low parts in tensor memory, over the chunk's S.  O += P_hi V + P_lo V (A from
-//    tensor memory, V as an MN-major operand straight from the ring), f32 in
-//    tensor memory.  The MMA warp computes the next chunk's scores while the
-//    row threads work on this one.
+//    high and low parts in tensor memory, over the chunk's S.
+//    O += P_hi V + P_lo V (A from tensor memory, V as an MN-major operand
+//    straight from the ring), f32 in tensor memory.  The score-MMA warp
+//    computes the next chunk's scores while the row threads work on this one.
 //  * A pair seen whole by one CTA is written normalised; otherwise the CTA
 //    stores an unnormalised partial with its (max, sum) per row in the layout
 //    of the split kernel's sub-groups of <= 16 rows, and the common merge
