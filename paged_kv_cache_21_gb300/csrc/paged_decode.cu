@@ -1401,6 +1401,121 @@ __global__ void __launch_bounds__(kMergeMaxThreads, 2) paged_decode_merge_kernel
     }
 }
 
+// One CTA per (sequence, KV head, query row): the row's partials are split
+// over the CTA's warps (warp w takes partials w, w + W, ...), each lane one
+// float4 column; every warp combines its partials with the running
+// (max, sum) rule, loading kMergeRowBatch of them at once, and the warps'
+// results are combined through shared memory.  Many partials per pair
+// (long contexts, wide groups) cost a few round trips instead of one per
+// few partials, and rows of one pair run on different SMs.
+constexpr int kMergeRowWarps = 4;
+constexpr int kMergeRowBatch = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeRowWarps * 32) paged_decode_merge_row_kernel(const MergeParams p)
+{
+    static_assert(D / 4 <= 32, "one float4 column per lane");
+    __shared__ float sM[kMergeRowWarps][32], sDen[kMergeRowWarps][32];
+    __shared__ float4 sAcc[kMergeRowWarps][32];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int row_g = blockIdx.x % p.G;
+    const int ph = blockIdx.x / p.G;
+    const int s = ph / p.Hkv, h = ph - s * p.Hkv;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const bool live = lane < D / 4;
+    const size_t row = (size_t)s * p.Hq + (size_t)h * p.G + row_g;
+    int L;
+    seq_blocks(p.ctx, s, p.max_blocks, L, row_g == 0 && t == 0);
+    if (p.nc > 0 && h == 0 && row_g == 0 && t == 0) {
+        int c, j, lead, members;
+        prefix_of(p.chunk, p.seq_chunk, p.nc, p.B, p.G, p.max_blocks, s, L, c, j, true);
+        if (s < p.nc) chunk_blocks(p.chunk, s, p.B, p.G, p.max_blocks, lead, members, true);
+    }
+    if (L <= 0) {
+        if (warp == 0 && live) store4(p, row * D + 4 * lane, 0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const int pair = (p.nc + s) * p.Hkv + h;
+    const int4 mt = p.pair_meta[pair];
+    const int na = mt.y;
+    if (mt.x < 0 || na < 1 || (long long)mt.x + na > (long long)p.nslots) return;
+    int nb = 0, crow = 0;
+    long long cslot0 = 0;
+    if (mt.z >= 0 && (mt.z >> 4) < p.nc) {
+        const int cpair = (mt.z >> 4) * p.Hkv + h;
+        const int4 cm = p.pair_meta[cpair];
+        if (cm.x < 0 || cm.y < 1 || (long long)cm.x + cm.y > (long long)p.nslots ||
+            (mt.z & 15) * p.G + p.G > p.prow)
+            return;
+        nb = cm.y;
+        cslot0 = cm.x;
+        crow = (mt.z & 15) * p.G;
+    }
+    if (na <= 1 && nb == 0) return;
+    const long long aslot0 = mt.x;
+    const int n = na + nb;
+    auto prow_of = [&](int k) -> size_t {
+        return k < na ? (size_t)(aslot0 + k) * p.prow + row_g
+                      : (size_t)(cslot0 + (k - na)) * p.prow + crow + row_g;
+    };
+    float M = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = warp; k0 < n; k0 += kMergeRowWarps * kMergeRowBatch) {
+        float2 v[kMergeRowBatch];
+        float4 ov[kMergeRowBatch];
+#pragma unroll
+        for (int e = 0; e < kMergeRowBatch; ++e) {
+            const int k = k0 + e * kMergeRowWarps;
+            if (k < n) {
+                const size_t r = prow_of(k);
+                v[e] = __ldcg(&p.part_ml[r]);
+                if (live) ov[e] = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D) + lane);
+            }
+        }
+        float bm = M;
+#pragma unroll
+        for (int e = 0; e < kMergeRowBatch; ++e)
+            if (k0 + e * kMergeRowWarps < n && v[e].y > 0.f) bm = fmaxf(bm, v[e].x);
+        const float rr = bm == -INFINITY ? 0.f : exp2f(M - bm);
+        den *= rr;
+        acc.x *= rr; acc.y *= rr; acc.z *= rr; acc.w *= rr;
+        M = bm;
+#pragma unroll
+        for (int e = 0; e < kMergeRowBatch; ++e) {
+            if (k0 + e * kMergeRowWarps < n && v[e].y > 0.f) {
+                const float f = exp2f(v[e].x - M);
+                den += f * v[e].y;
+                if (live) {
+                    acc.x += f * ov[e].x;
+                    acc.y += f * ov[e].y;
+                    acc.z += f * ov[e].z;
+                    acc.w += f * ov[e].w;
+                }
+            }
+        }
+    }
+    sM[warp][lane] = M;
+    sDen[warp][lane] = den;
+    sAcc[warp][lane] = acc;
+    __syncthreads();
+    if (warp != 0 || !live) return;
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeRowWarps; ++w) Mt = fmaxf(Mt, sM[w][lane]);
+    float dt = 0.f;
+    float4 at = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kMergeRowWarps; ++w) {
+        const float f = sM[w][lane] == -INFINITY ? 0.f : exp2f(sM[w][lane] - Mt);
+        dt += f * sDen[w][lane];
+        const float4 a = sAcc[w][lane];
+        at.x += f * a.x; at.y += f * a.y; at.z += f * a.z; at.w += f * a.w;
+    }
+    const float inv = dt > 0.f ? 1.f / dt : 0.f;
+    store4(p, row * D + 4 * lane, at.x * inv, at.y * inv, at.z * inv, at.w * inv);
+}
+
 // ------------------------------------------------------------------- host
 
 namespace {
@@ -1868,11 +1983,26 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     mp.max_blocks = max_blocks_per_seq;
     mp.nslots = (num_seqs + nc) * Hkv_v + slot_warps;
     mp.out_f32 = dp.out_f32;
-    const unsigned mgrid = (unsigned)(num_seqs * Hkv_v);
-    const unsigned mthreads = (unsigned)merge_threads(dp.G, head_dim);
-    err = head_dim == 128
-              ? launch_pdl(paged_decode_merge_kernel<128>, mgrid, mthreads, 0, st, mp)
-              : launch_pdl(paged_decode_merge_kernel<64>, mgrid, mthreads, 0, st, mp);
+    // one CTA per (sequence, KV head) while that fills the GPU; fewer pairs
+    // than SMs (long contexts at small batch: many partials per pair) take
+    // one CTA per query row, as long as those are at most two per SM (more,
+    // small CTAs cost more to schedule than the split of each pair's
+    // partials saves: measured on 64-row MQA, 32 x 8193)
+    const int msms = num_sms_current();
+    const int mpairs = num_seqs * Hkv_v;
+    if (mpairs >= msms || mpairs * dp.G > 2 * msms) {
+        const unsigned mgrid = (unsigned)(num_seqs * Hkv_v);
+        const unsigned mthreads = (unsigned)merge_threads(dp.G, head_dim);
+        err = head_dim == 128
+                  ? launch_pdl(paged_decode_merge_kernel<128>, mgrid, mthreads, 0, st, mp)
+                  : launch_pdl(paged_decode_merge_kernel<64>, mgrid, mthreads, 0, st, mp);
+    } else {
+        const unsigned mgrid = (unsigned)(num_seqs * Hkv_v * dp.G);
+        const unsigned mthreads = (unsigned)(kMergeRowWarps * 32);
+        err = head_dim == 128
+                  ? launch_pdl(paged_decode_merge_row_kernel<128>, mgrid, mthreads, 0, st, mp)
+                  : launch_pdl(paged_decode_merge_row_kernel<64>, mgrid, mthreads, 0, st, mp);
+    }
     if (err != cudaSuccess) return KV_ERR_CUDA;
     if (ev_end && cudaEventRecord(static_cast<cudaEvent_t>(ev_end), st) != cudaSuccess)
         return KV_ERR_CUDA;
