@@ -26,7 +26,7 @@
 //    stages form one contiguous operand) and does the fused append; warp 5
 //    allocates tensor memory and issues the score MMAs, warp 6 the P.V MMAs;
 //    warps 0-3 own one query row per thread (softmax and output).
-//  * Units are consumed in chunks of up to 4 blocks of one (sequence, head)
+//  * Units are consumed in chunks of up to 3 blocks of one (sequence, head)
 //    pair.  S = Q K^T: M = 128 query rows (the group, padded), N = 16 keys
 //    per block of the chunk in one MMA per 16-wide k-step, K = 128, f32 in
 //    tensor memory.  Each row thread loads its row of S (no shuffles),
@@ -63,18 +63,23 @@ namespace {
 
 constexpr int D = 128;
 constexpr int kRows = 128;                      // M of every MMA
-constexpr int kChunk = 4;                       // blocks per chunk
+constexpr int kChunk = 3;                       // blocks per chunk
 constexpr int kKeys = kChunk * kBlock;          // keys per chunk (S columns)
 constexpr int kBox = kBlock * 128;              // one box: 16 rows x 128 bytes
 constexpr uint32_t kTmemCols = 256;
-// tensor memory: buffer b at columns 64b holds S of a chunk (64 keys, f32),
-// then, in place, its P (32 columns of bf16 pairs for the high parts, then 32
-// for the low parts); O at columns 128-255
+// tensor memory: buffer b at columns 64b holds S of a chunk (48 keys, f32),
+// then, in place, its P (bf16 pairs: the high parts from column 64b, the low
+// parts from 64b + 32); O at columns 128-255.  Three blocks per chunk rather
+// than four: the chunks in the score/softmax/P.V chain hold six ring stages
+// instead of eight, so three more blocks are in flight (measured: 64 rows
+// 51.1 -> 47.9 us, 128 rows 62.9 -> 57.9 us at 32 x 8193; two blocks per
+// chunk: 53.2 and 61.6).
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
 constexpr int kThreads = 224;                   // 7 warps
 constexpr long long kWaitLimit = 1LL << 31;    // ~1 s of SM clocks
 constexpr uint32_t kIdescPV = umma::idesc_bf16_f32(kRows, D, false, true);
+static_assert(kKeys == 48, "P stores: one 32-key half, then a 16-key group");
 
 // Shared-memory layout for a Q buffer of QR rows (the group's rows, 64 or
 // 128; the 128-row MMAs read rows past QR from the memory that follows, and
@@ -627,9 +632,10 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (!ok) break;
             umma::fence_after_sync();
             uint32_t sr[kKeys];
-            umma::tmem_ld32(trow + kColS + (uint32_t)(64 * b), *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            umma::tmem_ld32(trow + kColS + (uint32_t)(64 * b + 32),
-                            *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+#pragma unroll
+            for (int c0 = 0; c0 < kKeys; c0 += 16)
+                umma::tmem_ld16(trow + kColS + (uint32_t)(64 * b + c0),
+                                *reinterpret_cast<uint32_t(*)[16]>(&sr[c0]));
             umma::tmem_wait_ld();
             const bool more = i + n < cnt;
             // Q is no longer read once this chunk's scores exist: load the
@@ -726,6 +732,25 @@ paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 umma::tmem_st16(trow + kColS + (uint32_t)(64 * b + 16 * half), hi);
                 umma::tmem_st16(trow + kColS + (uint32_t)(64 * b + 32 + 16 * half), lo);
+            }
+            if constexpr (kKeys % 32 == 16) {
+                // the last 16 keys: 8 columns at a 16-column boundary of each part
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int cc = kKeys - 16 + 2 * e;
+                    float p0 = ex2(fmaf(x[cc], sl2, nm));
+                    float p1 = ex2(fmaf(x[cc + 1], sl2, nm));
+                    if (!full) {
+                        p0 = x[cc] == -INFINITY ? 0.f : p0;
+                        p1 = x[cc + 1] == -INFINITY ? 0.f : p1;
+                    }
+                    ls[e & 3] += p0 + p1;
+                    hi[e] = pack_bf16x2(p0, p1);
+                    lo[e] = pack_bf16x2(p0 - bf16_lo(hi[e]), p1 - bf16_hi(hi[e]));
+                }
+                umma::tmem_st8(trow + kColS + (uint32_t)(64 * b + (kKeys - 16) / 2), hi);
+                umma::tmem_st8(trow + kColS + (uint32_t)(64 * b + 32 + (kKeys - 16) / 2), lo);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             umma::tmem_wait_st();
