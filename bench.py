@@ -420,6 +420,17 @@ def read_ceiling(pk, device, stream, nbytes=1 << 30, reps=10):
                                "read only; mean of %d launches" % reps}
 
 
+def split_kernel_name(case):
+    """The kernel the plain step (no prefix chunks) runs for the attention part:
+    the tcgen05 group kernel for bf16, head dim 128 and 64 or more query heads per
+    KV head, else the mma.sync split kernel."""
+    wide = case.D == 128 and case.kv_dtype == workloads.BF16 and case.Hq // case.Hkv >= 64
+    if wide:
+        return "paged_decode_wide_kernel<%d> (tcgen05)" % (64 if case.Hq // case.Hkv <= 64 else 128)
+    return "paged_decode_split_kernel<%d,%s> (mma.sync)" % (
+        case.D, "bf16" if case.kv_dtype == workloads.BF16 else "e4m3")
+
+
 def per_config(pk, cfgs, device, stream, K, W, world, peak, read_gbs):
     """Each of the other workloads on its own: fused step time, split and
     merge durations in the same loop mode, KV GB/s and the fractions of the
@@ -438,9 +449,7 @@ def per_config(pk, cfgs, device, stream, K, W, world, peak, read_gbs):
         gbs = kvb / (ms * 1e-3) / 1e9
         split_gbs = kvb / (m["split_ms"] * 1e-3) / 1e9
         r = {"config": workload_config(cfg), "us_per_step": ms * 1e3,
-             "kernel": ("paged_decode_wide_kernel (tcgen05)" if case.D == 128 and case.kv_dtype ==
-                        workloads.BF16 and case.Hq // case.Hkv >= 64 else
-                        "paged_decode_split_kernel (mma.sync)"),
+             "kernel": split_kernel_name(case),
              "kv_bytes_per_step": kvb, "kv_gbs": gbs,
              "frac_of_copy_peak": gbs / peak, "frac_of_read_ceiling": gbs / read_gbs,
              "split_us": m["split_ms"] * 1e3, "merge_us": m["merge_ms"] * 1e3,
@@ -752,8 +761,7 @@ def run_ours(args):
                if TRAFFIC["kernel_sha256"] == kernel_sha() and cfg == "2" and not args.batch
                else None)
     roofline = {"bound": "hbm",
-                "kernel": "paged_decode_split_kernel<%d,%s>" % (
-                    D, "bf16" if case.kv_dtype == workloads.BF16 else "e4m3"),
+                "kernel": split_kernel_name(case),
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
