@@ -51,3 +51,19 @@ def test_bench_cli_defaults_single_gpu():
     import bench
     a = bench.parse_args([])
     assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours" and a.config == "2"
+
+
+def test_kernel_named_for_each_workload():
+    """The roofline names the kernel the step runs: the tcgen05 group kernel for
+    bf16, d128 and 64+ query heads per KV head, else the mma.sync split kernel."""
+    import bench
+    import workloads
+    names = {}
+    for cfg in ("1", "2", "4", "5a", "5b", "mqa64", "mqa128"):
+        case = workloads.make_case(cfg, device="cpu", override={"B": 1})
+        names[cfg] = bench.split_kernel_name(case)
+    assert names["2"] == "paged_decode_split_kernel<128,bf16> (mma.sync)"
+    assert names["5a"] == "paged_decode_split_kernel<128,e4m3> (mma.sync)"
+    assert names["mqa64"] == "paged_decode_wide_kernel<64> (tcgen05)"
+    assert names["mqa128"] == "paged_decode_wide_kernel<128> (tcgen05)"
+    assert all("split_kernel" in names[c] for c in ("1", "4", "5b"))
