@@ -420,18 +420,20 @@ int kv_prefix_chunks(const int32_t* block_tables, int max_blocks_per_seq,
 
 /* kv_prefix_chunks with the decision whether the chunks pay (host memory):
  * returns the chunk table kv_prefix_chunks builds (group_size = num_q_heads /
- * num_kv_heads, min_blocks 1) when its chunks save at least 6 % of the
- * blocks the step reads and the step has more (sequence, KV head) pairs than
- * the split-KV kernel has resident warps; otherwise *num_chunks = 0 and
- * seq_chunk all -1, i.e. plain decoding.  (Measured crossovers of this
- * implementation: below either bound the shared-prefix kernel, which carries
- * two row tiles of state, is slower than reading the shared blocks once per
- * sequence -- which, with few pairs, mostly hit L2 anyway.)  resident_warps:
- * the split kernel's warps, or <= 0 to query the current device (152 SMs x 2
- * CTAs x 4 warps = 1216 on GB300 at d128).  Groups of more than 8 query
- * heads per KV head always get plain decoding.  chunks: num_seqs / 2 rows;
- * seq_chunk: num_seqs entries.  Returns KV_OK, KV_ERR_INVALID_ARG,
- * KV_ERR_UNSUPPORTED (shape) or KV_ERR_CUDA (device query). */
+ * num_kv_heads, min_blocks 1) when its chunks save a large enough fraction f
+ * of the blocks the step reads for the step's P = num_seqs * num_kv_heads
+ * (sequence, KV head) pairs against the split-KV kernel's W resident warps:
+ * f >= 6 % when 5 P >= 2 W, f >= 30 % when W <= 5 P < 2 W, never when
+ * 5 P < W.  Otherwise *num_chunks = 0 and seq_chunk all -1, i.e. plain
+ * decoding.  (Measured crossovers of this implementation: below these bounds
+ * the shared-prefix kernel, which carries two row tiles of state, is slower
+ * than reading the shared blocks once per sequence -- which, with few pairs,
+ * mostly hit L2 anyway.)  resident_warps: W, or <= 0 to query the current
+ * device (152 SMs x 2 CTAs x 4 warps = 1216 on GB300 at d128).  Groups of more
+ * than 8 query heads per KV head always get plain decoding.  chunks:
+ * num_seqs / 2 rows; seq_chunk: num_seqs entries.  Returns KV_OK,
+ * KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED (shape) or KV_ERR_CUDA (device
+ * query). */
 int kv_prefix_plan(const int32_t* block_tables, int max_blocks_per_seq,
                    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                    int head_dim, int kv_dtype, int resident_warps, int32_t* chunks,

@@ -415,13 +415,22 @@ const char* kv_version(void) { return "pagedkv 0.1 sm_103a"; }
 namespace pkv {
 
 // Shared-prefix decoding trades a costlier kernel (two row tiles of state)
-// for fewer bytes.  Measured on GB300 (fused step, 32 query / 8 KV heads,
-// d128): it pays once the chunks save about 6 % of the blocks read or more,
-// and only when there are more (sequence, KV head) pairs than resident warps
-// -- with fewer, every pair starts at a warp's range start, the members of a
-// group read their shared blocks at about the same moment and the plain
-// kernel already finds them in L2.
+// for fewer bytes.  Whether it pays depends on the fraction f of the step's
+// block reads the chunks save and on how many (sequence, KV head) pairs the
+// step has against the split kernel's resident warps W.  Measured on GB300
+// (fused step, 32 query / 8 KV heads, d128, W = 1216; groups of 8 sequences
+// sharing a prompt of 32-256 blocks, lengths 4200-8192; f 6-50 %):
+//   128 pairs: slower at every f (0.83-0.92x);
+//   256 pairs: even at f = 6 % and 25 %, slower at 13 %, faster from 38 %
+//              (1.10x; 1.22x at 51 %);
+//   512 and 1024 pairs: faster at every f >= 6 % (1.02-1.77x);
+//   2048 pairs: faster from f = 7.6 %, even at 3 %, slower at 5 % with
+//              lengths spread over 16-32768.
+// With few pairs the members of a group read their shared blocks close
+// together and the plain kernel finds most of them in L2.  The rule: chunks
+// when 5 pairs >= 2 W and f >= 6 %, or when 5 pairs >= W and f >= 30 %.
 constexpr double kPrefixMinSavedFraction = 0.06;
+constexpr double kPrefixMinSavedFractionFewPairs = 0.30;
 
 int prefix_plan_host(const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* context_lens, int num_seqs, int group_size,
@@ -454,7 +463,10 @@ int prefix_plan_host(const int32_t* block_tables, int max_blocks_per_seq,
         total += (L + KV_BLOCK_SIZE - 1) / KV_BLOCK_SIZE;
     }
     const long long pairs = (long long)num_seqs * num_kv_heads;
-    if ((double)saved >= kPrefixMinSavedFraction * (double)total && pairs > resident_warps) {
+    const double f_min = 5 * pairs >= 2LL * resident_warps ? kPrefixMinSavedFraction
+                         : 5 * pairs >= (long long)resident_warps ? kPrefixMinSavedFractionFewPairs
+                                                                  : 2.0;   // never
+    if ((double)saved >= f_min * (double)total) {
         *num_chunks = nc;
         return KV_OK;
     }

@@ -172,32 +172,61 @@ def _saved_fraction(chunks, lens):
     return saved / float((-(-np.asarray(lens, dtype=np.int64) // 16)).sum())
 
 
+def _plan_pays(frac, pairs, warps):
+    if 5 * pairs >= 2 * warps:
+        return frac >= 0.06
+    if 5 * pairs >= warps:
+        return frac >= 0.30
+    return False
+
+
 @pytest.mark.parametrize("cfg,override,want_chunks", [
     ("3", None, False),                 # 608-token prompt: ~5 % of the blocks saved
     ("3L", None, True),                 # 4096-token prompt: about half saved
-    ("3L", {"B": 32}, False),           # 256 pairs: fewer than the resident warps
     ("3L", {"B": 256, "prefix_blocks": 64}, True),
-    ("3L", {"B": 256, "prefix_blocks": 16}, False),
+    ("3L", {"B": 256, "prefix_blocks": 16}, False),                # ~3 % saved
+    ("3L", {"B": 128, "prefix_blocks": 32}, True),                 # 1024 pairs, ~6 %
+    ("3L", {"B": 64, "prefix_blocks": 32}, True),                  # 512 pairs, ~6 %
+    ("3L", {"B": 32}, True),                                       # 256 pairs, ~51 %
+    ("3L", {"B": 32, "prefix_blocks": 192}, True),                 # 256 pairs, ~38 %
+    ("3L", {"B": 32, "prefix_blocks": 128}, False),                # 256 pairs, ~25 %
+    ("3L", {"B": 16}, False),                                      # 128 pairs
 ])
 def test_plan_uses_chunks_only_where_they_pay(pk, cfg, override, want_chunks):
-    """kv_prefix_plan keeps kv_prefix_chunks' table when it saves >= 6 % of
-    the blocks read and the step has more (sequence, KV head) pairs than the
-    1216 resident warps of a GB300 (152 SMs x 2 CTAs x 4 warps); otherwise it
-    asks for plain decoding (no chunks, seq_chunk all -1)."""
+    """kv_prefix_plan keeps kv_prefix_chunks' table when the chunks save a
+    fraction f of the blocks read of at least 6 % (5 pairs >= 2 W) or 30 %
+    (W <= 5 pairs < 2 W), W = the 1216 resident warps of a GB300 (152 SMs x 2
+    CTAs x 4 warps); otherwise it asks for plain decoding (no chunks, seq_chunk
+    all -1)."""
     spec, L, bt, NB, _, _ = workloads.make_layout(cfg, override=override)
     G = spec["Hq"] // spec["Hkv"]
     full = pk.prefix_chunks(bt, L, G)
     chunks, seq_chunk = pk.prefix_plan(bt, L, spec["Hq"], spec["Hkv"], spec["D"],
                                        resident_warps=1216)
     frac = _saved_fraction(full[0], L)
-    pays = frac >= 0.06 and spec["B"] * spec["Hkv"] > 1216
-    assert pays == want_chunks, frac
+    assert _plan_pays(frac, spec["B"] * spec["Hkv"], 1216) == want_chunks, frac
     if want_chunks:
         np.testing.assert_array_equal(chunks, full[0])
         np.testing.assert_array_equal(seq_chunk, full[1])
         check_table(bt, L, G, chunks, seq_chunk)
     else:
         assert len(full[0]) > 0 and len(chunks) == 0 and (seq_chunk == -1).all()
+
+
+def test_plan_thresholds_follow_the_resident_warps(pk):
+    """The same tables planned for a device with other resident warps: the
+    tier boundaries move with W (5 pairs against W and 2 W)."""
+    spec, L, bt, NB, _, _ = workloads.make_layout("3L", override={"B": 32, "prefix_blocks": 64})
+    G = spec["Hq"] // spec["Hkv"]
+    frac = _saved_fraction(pk.prefix_chunks(bt, L, G)[0], L)
+    assert 0.06 <= frac < 0.30
+    pairs = spec["B"] * spec["Hkv"]                       # 256
+    for warps, want in ((5 * pairs // 2, True), (5 * pairs // 2 + 1, False),
+                        (5 * pairs, False), (5 * pairs + 1, False)):
+        chunks, seq_chunk = pk.prefix_plan(bt, L, spec["Hq"], spec["Hkv"], spec["D"],
+                                           resident_warps=warps)
+        assert (len(chunks) > 0) == want, warps
+        assert want or (seq_chunk == -1).all()
 
 
 def test_plan_refuses_large_groups_and_bad_shapes(pk):
