@@ -1246,6 +1246,7 @@ struct MergeParams {
     int prow;                // rows per partial slot
     int nslots;              // partial slots in the workspace
     int out_f32;
+    int early;               // context lengths are stable inputs: read them before the wait
 };
 
 // One CTA per (sequence, KV head): merge the partials the split kernel left
@@ -1270,18 +1271,20 @@ template <int D>
 __global__ void __launch_bounds__(kMergeMaxThreads, 2) paged_decode_merge_kernel(const MergeParams p)
 {
     __shared__ float2 sml[kMergeChunk * kMergeRows];
-    // the next kernel may start only once the split kernel (and with it the
-    // step's appends to the cache) is complete: a following call that reads
-    // its inputs early sees them
-    pdl_wait();
-    pdl_launch_dependents();
     const int s = blockIdx.x / p.Hkv, h = blockIdx.x - s * p.Hkv;
     const int t = threadIdx.x;
     const int nthr = blockDim.x;
     const int cols = p.G * (D / 4);
     const size_t row = (size_t)s * p.Hq + (size_t)h * p.G;
-    int L;
-    seq_blocks(p.ctx, s, p.max_blocks, L, true);
+    // with early inputs the length is read while the split kernel drains
+    int L = 0;
+    if (p.early) seq_blocks(p.ctx, s, p.max_blocks, L, true);
+    // the next kernel may start only once the split kernel (and with it the
+    // step's appends to the cache) is complete: a following call that reads
+    // its inputs early sees them
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!p.early) seq_blocks(p.ctx, s, p.max_blocks, L, true);
     if (p.nc > 0 && h == 0 && t == 0) {
         // report inconsistent prefix-chunk entries (the split kernel only reads)
         int c, j, lead, members;
@@ -1417,16 +1420,17 @@ __global__ void __launch_bounds__(kMergeRowWarps * 32) paged_decode_merge_row_ke
     static_assert(D / 4 <= 32, "one float4 column per lane");
     __shared__ float sM[kMergeRowWarps][32], sDen[kMergeRowWarps][32];
     __shared__ float4 sAcc[kMergeRowWarps][32];
-    pdl_wait();
-    pdl_launch_dependents();
     const int row_g = blockIdx.x % p.G;
     const int ph = blockIdx.x / p.G;
     const int s = ph / p.Hkv, h = ph - s * p.Hkv;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const bool live = lane < D / 4;
     const size_t row = (size_t)s * p.Hq + (size_t)h * p.G + row_g;
-    int L;
-    seq_blocks(p.ctx, s, p.max_blocks, L, row_g == 0 && t == 0);
+    int L = 0;
+    if (p.early) seq_blocks(p.ctx, s, p.max_blocks, L, row_g == 0 && t == 0);
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!p.early) seq_blocks(p.ctx, s, p.max_blocks, L, row_g == 0 && t == 0);
     if (p.nc > 0 && h == 0 && row_g == 0 && t == 0) {
         int c, j, lead, members;
         prefix_of(p.chunk, p.seq_chunk, p.nc, p.B, p.G, p.max_blocks, s, L, c, j, true);
@@ -1983,6 +1987,7 @@ int decode_launch(void* out, int out_dtype, const void* q, const void* k_cache,
     mp.max_blocks = max_blocks_per_seq;
     mp.nslots = (num_seqs + nc) * Hkv_v + slot_warps;
     mp.out_f32 = dp.out_f32;
+    mp.early = dp.early;
     // one CTA per (sequence, KV head) while that fills the GPU; fewer pairs
     // than SMs (long contexts at small batch: many partials per pair) take
     // one CTA per query row, as long as those are at most two per SM (more,
