@@ -422,10 +422,10 @@ def read_ceiling(pk, device, stream, nbytes=1 << 30, reps=10):
 
 def split_kernel_name(case):
     """The kernel the plain step (no prefix chunks) runs for the attention part:
-    the tcgen05 group kernel for bf16, head dim 128 and 64 or more query heads per
-    KV head, else the mma.sync split kernel."""
+    the tcgen05 group kernel for bf16, head dim 128 and more than 32 query heads
+    per KV head, else the mma.sync split kernel."""
     import workloads
-    wide = case.D == 128 and case.kv_dtype == workloads.BF16 and case.Hq // case.Hkv >= 64
+    wide = case.D == 128 and case.kv_dtype == workloads.BF16 and case.Hq // case.Hkv > 32
     if wide:
         return "paged_decode_wide_kernel<%d> (tcgen05)" % (64 if case.Hq // case.Hkv <= 64 else 128)
     return "paged_decode_split_kernel<%d,%s> (mma.sync)" % (

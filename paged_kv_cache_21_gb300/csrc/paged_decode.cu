@@ -1749,14 +1749,16 @@ struct LaunchPlan {
     WsLayout ws;
 };
 
-// Groups of 64 or more query rows per KV head on a bf16 cache with head_dim
-// 128 run the wide-group kernel (5th-generation tensor cores, all rows of a
-// group in one 128-row MMA); it writes its partials in the sub-group layout
-// below, so the same merge kernel follows.  Measured on GB300 (32 sequences
-// x 8193 tokens, one KV head, fused step): 128 rows 63.6 us against 108.9 us
-// for the sub-group kernel, 64 rows 54.1 against 61.5; at 32 rows the
-// sub-group kernel is faster (38.4 against 49.4 us).
-constexpr int kWideMinRows = 64;
+// Groups of more than 32 query rows per KV head (four or more sub-groups) on
+// a bf16 cache with head_dim 128 run the wide-group kernel (5th-generation
+// tensor cores, all rows of a group in one 128-row MMA); it writes its
+// partials in the sub-group layout below, so the same merge kernel follows.
+// Measured on GB300 (32 sequences x 8193 tokens, one KV head, fused step):
+// 128 rows 57.7 us against 108.9 us for the sub-group kernel, 64 rows 47.6
+// against 61.5, 48 rows 51.8 against 60.5; at 32 rows and below the sub-group
+// kernel is faster (32 rows 38.5 against 41.5 us, 24 rows 37.5 against 44.4;
+// 32 rows at 64 x 16385, 8 x 32769 and 128 x 2049 tokens likewise).
+constexpr int kWideMinRows = 33;
 
 bool use_wide(int Hq, int Hkv, int D, bool fp8, int nc)
 {

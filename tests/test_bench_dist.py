@@ -55,7 +55,8 @@ def test_bench_cli_defaults_single_gpu():
 
 def test_kernel_named_for_each_workload():
     """The roofline names the kernel the step runs: the tcgen05 group kernel for
-    bf16, d128 and 64+ query heads per KV head, else the mma.sync split kernel."""
+    bf16, d128 and more than 32 query heads per KV head, else the mma.sync split
+    kernel."""
     import bench
     import workloads
     names = {}

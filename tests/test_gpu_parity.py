@@ -239,12 +239,13 @@ LARGE_GROUP_LENS = [1, 17, 300, 4097, 2000, 33]
 @pytest.mark.parametrize("kv_dtype", [workloads.BF16, workloads.FP8_E4M3])
 @pytest.mark.parametrize("Hq,Hkv,D", [(12, 1, 128), (16, 2, 128), (24, 3, 128), (32, 1, 128),
                                       (48, 2, 64), (64, 1, 128), (128, 1, 64), (128, 1, 128),
-                                      (256, 2, 128), (80, 1, 128), (96, 1, 128), (72, 1, 128)])
+                                      (256, 2, 128), (80, 1, 128), (96, 1, 128), (72, 1, 128),
+                                      (40, 1, 128), (48, 1, 128), (96, 2, 128)])
 def test_large_query_groups(Hq, Hkv, D, kv_dtype):
     """G = 12..128, MQA on many-head models ("KV cache complete guide",
     section "(2) GQA": one KV head for all query heads): 9-16 rows run the
     two-row-tile kernel, larger groups run as 2, 4 or 8 sub-groups that read
-    the same KV tiles, and above 64 rows (bf16, d128) the tensor-memory
+    the same KV tiles, and above 32 rows (bf16, d128) the tensor-memory
     kernel takes the whole group in one 128-row MMA.  Two-launch and fused
     paths, float32 output, and the append lands once, bit-exact."""
     case = workloads.make_custom(len(LARGE_GROUP_LENS), Hq, Hkv, D, LARGE_GROUP_LENS,
@@ -255,7 +256,7 @@ def test_large_query_groups(Hq, Hkv, D, kv_dtype):
     check_case(case, what="f32 " + what, out_dtype=torch.float32)
 
 
-@pytest.mark.parametrize("Hq", [32, 64, 128])
+@pytest.mark.parametrize("Hq", [32, 48, 64, 128])
 def test_mqa_full_size_and_deterministic(Hq):
     """One KV head for Hq query heads at the 8B layer's batch and context
     (32 sequences x 8193 tokens, d128): every output against the oracle, and
@@ -270,10 +271,10 @@ def test_mqa_full_size_and_deterministic(Hq):
     assert pk.get_device_error()[0] == 0
 
 
-@pytest.mark.parametrize("Hq", [64, 128])
+@pytest.mark.parametrize("Hq", [48, 64, 128])
 @pytest.mark.parametrize("lens", [[100000], [30000, 1, 17, 20000]])
 def test_wide_groups_split_over_many_ctas(lens, Hq):
-    """64 or 128 query rows on one KV head with pairs cut across tens of CTAs
+    """48, 64 or 128 query rows on one KV head with pairs cut across tens of CTAs
     of the tensor-memory kernel (partials in sub-groups of 16 rows, then the
     merge), short pairs seen whole by one CTA beside them."""
     case = workloads.make_custom(len(lens), Hq, 1, 128, lens, seed=len(lens) + 77)
@@ -281,7 +282,7 @@ def test_wide_groups_split_over_many_ctas(lens, Hq):
     check_case(case, what="wide f32 %s" % lens, out_dtype=torch.float32)
 
 
-@pytest.mark.parametrize("Hq", [64, 128])
+@pytest.mark.parametrize("Hq", [48, 64, 128])
 def test_wide_groups_flag_bad_block_ids(Hq):
     """A block id outside the pool in the tensor-memory kernel is not
     fetched: its keys are masked, KV_DEVERR_BLOCK_OUT_OF_RANGE is raised with
