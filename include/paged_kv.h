@@ -518,8 +518,8 @@ int kv_read_ceiling(const void* buf, size_t bytes, unsigned* sink, void* stream)
  * on a barrier that nothing arrives on, gives up after `cycles` SM clocks
  * and takes the time-out path -- KV_DEVERR_PIPELINE_TIMEOUT raised, the bulk
  * copies it has issued waited for at the normal limit, the warp stops, so
- * that call's output is undefined.  In the wide-group kernel (groups of 64+
- * rows) the score-MMA warp of every CTA does so on its first wait, and every
+ * that call's output is undefined.  In the wide-group kernel (groups of more
+ * than 32 rows, bf16 cache, head_dim 128) the score-MMA warp of every CTA does so on its first wait, and every
  * role of the CTA then stops (copies and MMAs in flight are waited for and
  * tensor memory is freed before the CTA ends).  It lets a test see the flag without a
  * copy that really never arrives.  0 (the default) turns it off; a value

@@ -1744,7 +1744,7 @@ int check_shape(int num_seqs, int Hq, int Hkv, int D, int kv_dtype)
 // slots (a second set of per-warp slots for the prefix-chunk phase).
 struct LaunchPlan {
     HeadSplit hs;
-    bool wide;             // the tensor-memory kernel for groups above 16 rows
+    bool wide;             // the tensor-memory kernel (groups above 32 rows, see use_wide)
     int nr, grid, warps_total, slot_warps;
     WsLayout ws;
 };
