@@ -41,10 +41,10 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the split kernel (dram__bytes_read.sum + dram__bytes_write.sum)
 # per launch on this workload, with the hash of the kernel source it was
 # measured on; reported as null once the source has changed.
-TRAFFIC = {"kernel_sha256": "accd1b0969e6e310ca03f0f72f916d8dfe322af4bd0ee9a76bde12eafd44f76e",
-           "bytes_per_launch": 1087600640,
+TRAFFIC = {"kernel_sha256": "ceed717c42f2174b1ae20a9d9026475580e9c33fc6a116eeda5e011d810deaf1",
+           "bytes_per_launch": 1086476288,
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the batch-8 launch "
-                     "(269,147,648 B + 2,752,512 B), scaled x4 by units processed "
+                     "(269,147,648 B + 2,471,424 B), scaled x4 by units processed "
                      "(profiles/smem_bank_conflicts_split_b8.md)"}
 
 
